@@ -1,0 +1,169 @@
+/*
+ * tq.h - C ABI of the TurboQuant compressed KV-cache library for NVIDIA B300 (sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * Online KV-cache compression as described in
+ *   [BLOG]  "Технология TurboQuant и её применение с локальными LLM" (ast-softpro.ru),
+ *           section 1.2 "Как работает TurboQuant";
+ *   [3BITS] "3 бита вместо 16: разбираем TurboQuant и когда его реально стоит включать"
+ *           (kiosknews.app), section "Как работает TurboQuant" and section
+ *           "Python + HuggingFace" (quantize returns indices and norms per vector).
+ *
+ *   key x (d coordinates, bf16):   n = ||x||,  y = Pi x,  idx_j = #{k : y_j / n >= t_k}
+ *                                  (Lloyd-Max codebook with 2^(b-1) levels),
+ *                                  r = x - n Pi^T c[idx],  gamma = ||r||,
+ *                                  sigma_i = [ (S r)_i >= 0 ]  (QJL sign sketch, m = d)
+ *   value v (bf16):                n_v = ||v||, idx over a 2^b-level codebook, no QJL.
+ *   decode, query q, kv head g = floor(h / G):
+ *       logit_t = ( n_t <Pi q, c_K[idx_t]> + gamma_t sqrt(pi/2)/m <S q, 2 sigma_t - 1> ) / sqrt(d)
+ *       out     = Pi^T sum_t softmax(logit)_t n_v,t c_V[idx_v,t]
+ *
+ * Pi is a Haar-random orthogonal d x d matrix (QR of a seeded Gaussian matrix with the
+ * signs of R's diagonal moved into Q), S an m x d matrix of i.i.d. N(0,1) entries, both
+ * drawn from SplitMix64 + Box-Muller streams seeded with 2*seed and 2*seed+1.  The
+ * codebooks are the Lloyd-Max quantizers of the exact density of one coordinate of a
+ * uniform unit vector in R^d, (1 - t^2)^((d-3)/2) on [-1, 1]: data-oblivious, computed
+ * once per (d, levels) on the host ([3BITS]: the codebook is stored, no calibration).
+ *
+ * Conventions
+ * -----------
+ * - Every function returns TQ_OK (0) or a negative TQ_E* code; nothing throws.
+ * - Device pointers are plain CUDA device addresses on the context's device; the caller
+ *   owns and allocates them (e.g. with PyTorch).  The library owns only the context's
+ *   constant buffers (Pi, S, S Pi^T, codebooks, a status word).
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous on
+ *   that stream and never synchronise the host, except tq_get_device_status.
+ * - Supported: d in {64, 128, 256}, bits b in {2, 3, 4, 5}, m == d.
+ * - Errors the host cannot see (a start position or sequence length read from device
+ *   memory that exceeds max_tokens) make the kernels skip the offending work and set a
+ *   sticky flag that tq_get_device_status reports.
+ *
+ * Compressed cache layout, format version 1
+ * -----------------------------------------
+ * cache = [batch][kv_head][page][page_bytes], P = TQ_PAGE_TOKENS = 128 token slots per
+ * page; token t of a sequence lives in page t / P, slot t % P.  Each page holds six
+ * regions, in this order (little-endian u32 words and f32 values):
+ *   1. key codes    [b-1 planes][P slots][d/32 words]  plane q carries bit q of each code
+ *   2. key signs    [P slots][m/32 words]              bit = sigma_i
+ *   3. key norm     [P] f32                             n
+ *   4. residual     [P] f32                             gamma
+ *   5. value codes  [b planes][d coords][4 words]      plane q carries bit q of each code
+ *   6. value norm   [P] f32                             n_v
+ * page_bytes = P * ((b-1) d/8 + m/8 + 8 + b d/8 + 4)   (13,824 B at d = 128, b = 3).
+ * Key codes and signs: within one slot's words, coordinate j is at
+ *     kb = j>>5, h = (j>>4)&1, c = (j>>2)&3, e = j&3, s = c*(2*D/32) + 2*kb + h,
+ *     word = s>>3, bit = (s&7) + 8*e          (D = d for codes, m for signs).
+ * Value codes: within one coordinate's 4 words, token slot tau is at
+ *     kb = tau>>5, h = (tau>>4)&1, c = (tau>>2)&3, e = tau&3, word = c, bit = 2*kb+h+8*e.
+ * (These permutations put the bits that one thread of an m16n8k32 tensor-core fragment
+ *  needs into one word.)  Slots not yet written hold arbitrary bytes; decode never reads
+ *  them as data.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_FORMAT_VERSION 1
+#define TQ_PAGE_TOKENS 128
+
+enum {
+  TQ_OK = 0,
+  TQ_EINVAL = -1,       /* bad argument (null pointer, negative size, misaligned buffer) */
+  TQ_EUNSUPPORTED = -2, /* d, bits, m or group size outside the supported set           */
+  TQ_ECUDA = -3,        /* a CUDA runtime call or kernel launch failed                   */
+  TQ_ETIMEOUT = -4,     /* a device-side bounded wait gave up (sticky device flag)       */
+  TQ_EBOUNDS = -5,      /* device-side position / length beyond max_tokens (sticky flag) */
+  TQ_ENOMEM = -6,       /* workspace too small, or a context allocation failed           */
+  TQ_ENOTCONV = -7      /* host codebook solver did not converge                        */
+};
+
+typedef struct tq_ctx tq_ctx;
+
+/* ---- host-only set-up (no GPU needed) ------------------------------------------- */
+
+/* Lloyd-Max codebook for one coordinate of a uniform unit vector in R^d ([BLOG] 1.2,
+ * stage 1; [3BITS] "idea two").  d >= 3, 2 <= levels <= 64.  Writes `levels` ascending
+ * centroids and `levels-1` interior boundaries (midpoints), fp64, into caller-owned host
+ * memory.  The book is exactly antisymmetric, so the middle boundary is 0. */
+int tq_make_codebook(int d, int levels, double* centroids, double* boundaries);
+
+/* Haar rotation Pi ([BLOG] 1.2, "random orthogonal rotation"), d x d row-major fp64 into
+ * caller-owned host memory; y = Pi x.  1 <= d <= 4096. */
+int tq_make_rotation(int d, uint64_t seed, double* pi_out);
+
+/* QJL projection S ([BLOG] 1.2, stage 2, "random Gaussian matrix"), m x d row-major fp64,
+ * i.i.d. N(0,1).  1 <= m, d <= 4096. */
+int tq_make_projection(int m, int d, uint64_t seed, double* s_out);
+
+/* ---- context -------------------------------------------------------------------- */
+
+/* Builds Pi, S, S Pi^T and both codebooks for (d, bits, m, seed) on the host and copies
+ * them to `device`.  Returns TQ_EUNSUPPORTED unless d in {64,128,256}, bits in 2..5 and
+ * m == d.  The context is immutable afterwards and may be shared by concurrent calls. */
+int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, tq_ctx** out);
+void tq_ctx_destroy(tq_ctx* ctx);
+
+/* Bytes of one page, and of a whole cache [batch][kv_heads][ceil(max_tokens/P)] pages
+ * (0 on a bad argument). */
+size_t tq_page_bytes(const tq_ctx* ctx);
+size_t tq_cache_bytes(const tq_ctx* ctx, int batch, int kv_heads, int max_tokens);
+
+/* Copies the context's fp64 host-side constants into caller buffers (any may be NULL):
+ * pi [d*d], s [m*d], key codebook [2^(b-1)] + boundaries [2^(b-1)-1], value codebook
+ * [2^b] + boundaries [2^b-1].  Used to cross-check the set-up against an independent
+ * implementation. */
+int tq_ctx_get_constants(const tq_ctx* ctx, double* pi, double* s, double* ck, double* tk,
+                         double* cv, double* tv);
+
+/* ---- hot path ------------------------------------------------------------------- */
+
+/* Quantizes n_tokens new key and value vectors per (batch, kv head) into the cache
+ * ([BLOG] 1.2 stages 1 and 2 for keys, stage 1 with b bits for values).
+ *   k, v       device bf16 [batch][kv_heads][n_tokens][d], contiguous, 16-byte aligned
+ *   start_pos  device int32 [batch]: slot of the first new token of each sequence; token i
+ *              goes to slot start_pos[b] + i.  Any alignment is allowed.
+ *   cache      device, tq_cache_bytes(ctx, batch, kv_heads, max_tokens) bytes, 256-byte
+ *              aligned; only the slots written are modified.
+ * If start_pos[b] < 0 or start_pos[b] + n_tokens > max_tokens, sequence b is skipped and
+ * the sticky TQ_EBOUNDS flag is set.  Calls that write the same page must be ordered. */
+int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
+                   int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
+                   void* stream);
+
+/* Scratch bytes tq_attn_decode needs for these sizes. */
+size_t tq_decode_workspace_bytes(const tq_ctx* ctx, int batch, int q_heads, int kv_heads,
+                                 int max_tokens);
+
+/* Decode attention over the compressed cache (one query per head).
+ *   q          device fp32 [batch][q_heads][d]
+ *   cache      as written by tq_quantize_kv, [batch][kv_heads][pages][page]
+ *   seq_lens   device int32 [batch]: attend to slots t < seq_lens[b]; 0 gives a zero row.
+ *              A value above max_tokens is clamped and sets the sticky TQ_EBOUNDS flag.
+ *   out        device fp32 [batch][q_heads][d]
+ *   logits_out NULL, or device fp32 [batch][q_heads][max_tokens]: receives every logit
+ *              t < seq_lens[b] (for testing; other entries untouched)
+ *   workspace  device scratch of at least tq_decode_workspace_bytes(...) bytes, 256-byte
+ *              aligned; its contents need no initialisation.
+ * q_heads must be a multiple of kv_heads (query head h reads kv head h / (q_heads/kv_heads)),
+ * with at most 16 query heads per kv head. */
+int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                   const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
+                   float* logits_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then returns and clears the sticky device status: TQ_OK,
+ * TQ_EBOUNDS or TQ_ETIMEOUT. */
+int tq_get_device_status(const tq_ctx* ctx, void* stream);
+
+const char* tq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */

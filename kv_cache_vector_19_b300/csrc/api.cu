@@ -1,0 +1,208 @@
+// C ABI of the library: context set-up, argument checks, kernel dispatch, status.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "tq_internal.h"
+
+namespace {
+
+bool supported(int d, int bits, int m) {
+  return (d == 64 || d == 128 || d == 256) && bits >= 2 && bits <= 5 && m == d;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int upload(const std::vector<double>& src, float** dst) {
+  std::vector<float> f(src.size());
+  for (size_t i = 0; i < src.size(); ++i) f[i] = (float)src[i];
+  if (cudaMalloc(reinterpret_cast<void**>(dst), f.size() * sizeof(float)) != cudaSuccess) return TQ_ENOMEM;
+  if (cudaMemcpy(*dst, f.data(), f.size() * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) return TQ_ECUDA;
+  return TQ_OK;
+}
+
+void release(tq_ctx* c) {
+  if (!c) return;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  cudaSetDevice(c->device);
+  float* bufs[] = {c->d_pi, c->d_pit, c->d_st, c->d_spt, c->d_ck, c->d_tk, c->d_cv, c->d_tv};
+  for (float* p : bufs)
+    if (p) cudaFree(p);
+  if (c->d_status) cudaFree(c->d_status);
+  if (prev >= 0) cudaSetDevice(prev);
+  delete c;
+}
+
+// Makes the context's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1, dev;
+  explicit DeviceGuard(int d) : dev(d) {
+    cudaGetDevice(&prev);
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0 && prev != dev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, tq_ctx** out) {
+  if (!out) return TQ_EINVAL;
+  *out = nullptr;
+  if (!supported(d, bits, m)) return TQ_EUNSUPPORTED;
+  tq_ctx* c = new (std::nothrow) tq_ctx();
+  if (!c) return TQ_ENOMEM;
+  c->d = d;
+  c->bits = bits;
+  c->m = m;
+  c->seed = seed;
+  c->device = device;
+  c->lk = 1 << (bits - 1);
+  c->lv = 1 << bits;
+  c->page_bytes = tq::page_bytes(d, bits, m);
+  c->pi.resize((size_t)d * d);
+  c->s.resize((size_t)m * d);
+  c->ck.resize(c->lk);
+  c->tk.resize(c->lk - 1);
+  c->cv.resize(c->lv);
+  c->tv.resize(c->lv - 1);
+  tq::haar_rotation(d, seed, c->pi.data());
+  tq::gaussian_projection(m, d, seed, c->s.data());
+  int rc = tq::lloyd_max(d, c->lk, c->ck.data(), c->tk.data());
+  if (rc == TQ_OK) rc = tq::lloyd_max(d, c->lv, c->cv.data(), c->tv.data());
+  if (rc != TQ_OK) {
+    delete c;
+    return rc;
+  }
+  // derived host matrices: Pi^T, S^T, (S Pi^T)^T
+  std::vector<double> pit((size_t)d * d), st((size_t)d * m), spt((size_t)d * m);
+  for (int i = 0; i < d; ++i)
+    for (int j = 0; j < d; ++j) pit[(size_t)j * d + i] = c->pi[(size_t)i * d + j];
+  for (int i = 0; i < m; ++i)
+    for (int k = 0; k < d; ++k) st[(size_t)k * m + i] = c->s[(size_t)i * d + k];
+  for (int i = 0; i < m; ++i)
+    for (int j = 0; j < d; ++j) {
+      double acc = 0.0;   // S'[i][j] = sum_k S[i][k] Pi[j][k]
+      for (int k = 0; k < d; ++k) acc += c->s[(size_t)i * d + k] * c->pi[(size_t)j * d + k];
+      spt[(size_t)j * m + i] = acc;
+    }
+  {
+    DeviceGuard guard(device);
+    rc = upload(c->pi, &c->d_pi);
+    if (rc == TQ_OK) rc = upload(pit, &c->d_pit);
+    if (rc == TQ_OK) rc = upload(st, &c->d_st);
+    if (rc == TQ_OK) rc = upload(spt, &c->d_spt);
+    if (rc == TQ_OK) rc = upload(c->ck, &c->d_ck);
+    if (rc == TQ_OK) rc = upload(c->tk, &c->d_tk);
+    if (rc == TQ_OK) rc = upload(c->cv, &c->d_cv);
+    if (rc == TQ_OK) rc = upload(c->tv, &c->d_tv);
+    if (rc == TQ_OK) {
+      if (cudaMalloc(&c->d_status, sizeof(int)) != cudaSuccess ||
+          cudaMemset(c->d_status, 0, sizeof(int)) != cudaSuccess)
+        rc = TQ_ECUDA;
+    }
+  }
+  if (rc != TQ_OK) {
+    release(c);
+    return rc;
+  }
+  *out = c;
+  return TQ_OK;
+}
+
+extern "C" void tq_ctx_destroy(tq_ctx* ctx) { release(ctx); }
+
+extern "C" size_t tq_page_bytes(const tq_ctx* ctx) { return ctx ? ctx->page_bytes : 0; }
+
+extern "C" size_t tq_cache_bytes(const tq_ctx* ctx, int batch, int kv_heads, int max_tokens) {
+  if (!ctx || batch < 1 || kv_heads < 1 || max_tokens < 1) return 0;
+  size_t pages = (size_t)(max_tokens + TQ_PAGE_TOKENS - 1) / TQ_PAGE_TOKENS;
+  return (size_t)batch * kv_heads * pages * ctx->page_bytes;
+}
+
+extern "C" int tq_ctx_get_constants(const tq_ctx* ctx, double* pi, double* s, double* ck, double* tk,
+                                    double* cv, double* tv) {
+  if (!ctx) return TQ_EINVAL;
+  auto cp = [](const std::vector<double>& v, double* dst) {
+    if (dst) std::memcpy(dst, v.data(), v.size() * sizeof(double));
+  };
+  cp(ctx->pi, pi);
+  cp(ctx->s, s);
+  cp(ctx->ck, ck);
+  cp(ctx->tk, tk);
+  cp(ctx->cv, cv);
+  cp(ctx->tv, tv);
+  return TQ_OK;
+}
+
+extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
+                              int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
+                              void* stream) {
+  if (!ctx || !k || !v || !start_pos || !cache) return TQ_EINVAL;
+  if (batch < 1 || kv_heads < 1 || n_tokens < 0 || max_tokens < 1) return TQ_EINVAL;
+  if (batch > 65535 || kv_heads > 65535) return TQ_EINVAL;
+  if (n_tokens > max_tokens) return TQ_EINVAL;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(cache, 256) || !aligned(start_pos, 4)) return TQ_EINVAL;
+  if (n_tokens == 0) return TQ_OK;
+  DeviceGuard guard(ctx->device);
+  return launch_quantize_simt(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
+}
+
+extern "C" size_t tq_decode_workspace_bytes(const tq_ctx* ctx, int batch, int q_heads, int kv_heads,
+                                            int max_tokens) {
+  if (!ctx || batch < 1 || q_heads < 1 || kv_heads < 1 || max_tokens < 1) return 0;
+  tq::SplitPlan sp = tq::plan_splits(batch, kv_heads, max_tokens);
+  size_t rows = (size_t)batch * q_heads;
+  size_t floats = rows * ctx->d * 2 + rows * sp.splits * (2 + ctx->d);
+  return floats * sizeof(float);
+}
+
+extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                              const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
+                              float* logits_out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ctx || !q || !cache || !seq_lens || !out || !workspace) return TQ_EINVAL;
+  if (batch < 1 || q_heads < 1 || kv_heads < 1 || max_tokens < 1) return TQ_EINVAL;
+  if (batch > 65535 || kv_heads > 65535 || q_heads > 65535) return TQ_EINVAL;
+  if (q_heads % kv_heads != 0) return TQ_EINVAL;
+  if (q_heads / kv_heads > 16) return TQ_EUNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(cache, 256) || !aligned(out, 16) || !aligned(workspace, 256) ||
+      !aligned(seq_lens, 4) || (logits_out && !aligned(logits_out, 4)))
+    return TQ_EINVAL;
+  if (workspace_bytes < tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens)) return TQ_ENOMEM;
+  DeviceGuard guard(ctx->device);
+  return launch_decode_simt(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
+                            workspace, stream);
+}
+
+extern "C" int tq_get_device_status(const tq_ctx* ctx, void* stream) {
+  if (!ctx) return TQ_EINVAL;
+  DeviceGuard guard(ctx->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int flags = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TQ_ECUDA;
+  if (cudaMemcpy(&flags, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ECUDA;
+  if (cudaMemset(ctx->d_status, 0, sizeof(int)) != cudaSuccess) return TQ_ECUDA;
+  if (flags & tq::kFlagTimeout) return TQ_ETIMEOUT;
+  if (flags & tq::kFlagBounds) return TQ_EBOUNDS;
+  return TQ_OK;
+}
+
+extern "C" const char* tq_status_string(int status) {
+  switch (status) {
+    case TQ_OK: return "ok";
+    case TQ_EINVAL: return "invalid argument";
+    case TQ_EUNSUPPORTED: return "unsupported head dim, bit width, projection size or group size";
+    case TQ_ECUDA: return "CUDA runtime error";
+    case TQ_ETIMEOUT: return "device-side wait timed out";
+    case TQ_EBOUNDS: return "device-side position or length beyond max_tokens";
+    case TQ_ENOMEM: return "allocation failed or workspace too small";
+    case TQ_ENOTCONV: return "codebook solver did not converge";
+    default: return "unknown status";
+  }
+}

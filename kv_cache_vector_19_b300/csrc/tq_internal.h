@@ -1,0 +1,58 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "tq.h"
+
+namespace tq {
+
+void gaussian_stream(uint64_t stream_seed, size_t count, double* out);
+void haar_rotation(int d, uint64_t seed, double* pi);
+void gaussian_projection(int m, int d, uint64_t seed, double* s);
+int lloyd_max(int d, int levels, double* centroids, double* boundaries);
+
+// Sticky device status bits (ORed by kernels into ctx->d_status).
+enum : int { kFlagBounds = 1, kFlagTimeout = 2 };
+
+constexpr int kPage = TQ_PAGE_TOKENS;
+
+inline size_t page_bytes(int d, int bits, int m) {
+  return (size_t)kPage * ((size_t)(bits - 1) * d / 8 + m / 8 + 8 + (size_t)bits * d / 8 + 4);
+}
+
+// Decode split plan shared by the workspace query and the launch.
+struct SplitPlan {
+  int pages, splits, pages_per_split;
+};
+SplitPlan plan_splits(int batch, int kv_heads, int max_tokens);
+
+}  // namespace tq
+
+struct tq_ctx {
+  int d, bits, m, device;
+  uint64_t seed;
+  int lk, lv;
+  size_t page_bytes;
+  std::vector<double> pi, s, ck, tk, cv, tv;   // fp64 host copies
+  // device constants, fp32
+  float* d_pi = nullptr;    // [d][d]  Pi, row-major
+  float* d_pit = nullptr;   // [d][d]  Pi^T
+  float* d_st = nullptr;    // [d][m]  S^T
+  float* d_spt = nullptr;   // [d][m]  (S Pi^T)^T
+  float* d_ck = nullptr;    // [lk]
+  float* d_tk = nullptr;    // [lk-1]
+  float* d_cv = nullptr;    // [lv]
+  float* d_tv = nullptr;    // [lv-1]
+  int* d_status = nullptr;  // sticky flags
+};
+
+// Kernel launchers (return TQ_OK or TQ_ECUDA).
+int launch_quantize_simt(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
+                         int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
+                         void* stream);
+int launch_decode_simt(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                       const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
+                       float* logits_out, void* workspace, void* stream);
