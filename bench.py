@@ -1,0 +1,441 @@
+"""Benchmark of the TurboQuant compressed-KV path on B300: prefill quantize + decode steps.
+
+One step = the whole hot path over one batch of the long-context workload (batch 4, 8 KV
+heads, 32 query heads, head_dim 128, b=3, 131,072 cached tokens per sequence):
+  1. tq_quantize_kv of the full prefill (524,288 tokens x 8 KV heads, K and V);
+  2. 64 decode steps, each appending one token per (sequence, KV head) with
+     tq_quantize_kv and then running tq_attn_decode for all 32 query heads.
+
+Printed (rank 0, one JSON line):
+  value       compressed-KV decode GB/s: algorithmic bytes of the 64 decode steps (the
+              compressed pages attended, plus q and out) over the device time of the decode
+              phase (appends included), summed over all ranks' work / max-over-ranks time;
+  quantize_mtok_s  prefill tokens (all KV heads of a token) per second;
+  roofline    the decode kernel's algorithmic GB/s against the measured HBM copy peak;
+  e2e         the same metric with the step's inputs copied from pinned host memory and
+              the step's outputs read back, inside the timed region;
+  cpu_baseline  the fp64 oracle on a bounded sample of the same workload, host cores.
+
+--impl reference times the oracle alone (there is no other implementation of this path).
+--sweep prints one line per (d, b) point of the bit/dim sweep instead.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "compressed-KV decode GB/s & % HBM roofline; quantize Mtokens/s (d=128, b=3)"
+UNIT = "GB/s"
+# dram__bytes_read.sum + dram__bytes_write.sum per decode launch, from the ncu capture of
+# the current decode kernels on this workload (None until captured for the current code).
+DECODE_TRAFFIC_BYTES = None
+
+
+def bpt(d, b, m):
+    """Compressed bytes per token per KV head (keys + values)."""
+    return (b - 1) * d // 8 + m // 8 + 8 + b * d // 8 + 4
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(w, seconds=12.0, reps_max=1000):
+    """The oracle's own decode over packed pages (unpack + route A for the G query heads
+    of one KV head) on a 1024-token sample of the workload, repeated for ~`seconds`.
+    Returns (GB/s of compressed pages decoded, Mtokens/s quantized, threads, description)."""
+    import numpy as np
+    from threadpoolctl import threadpool_info
+
+    from oracle import decode as odec
+    from oracle import pagefmt, params, quant
+
+    rng = np.random.default_rng(1234)
+    d, b, m, G = w.d, w.b, w.m, w.group
+    T = 1024
+    p = params.make(d, b, m, seed=w.seed)
+    X = rng.standard_normal((2, T, d)).astype(np.float32)
+    import torch
+    X = torch.from_numpy(X).to(torch.bfloat16).double().numpy()
+    t0 = time.perf_counter()
+    ok = quant.quantize_keys(X[0], p.Pi, p.S, p.cb_k)
+    ov = quant.quantize_values(X[1], p.Pi, p.cb_v)
+    t_quant = time.perf_counter() - t0
+    pages = []
+    for pg in range(T // 128):
+        s = slice(pg * 128, (pg + 1) * 128)
+        pages.append(pagefmt.pack_page(d, b, m, ok["idx"][s], ok["sigma"][s], ok["n"][s], ok["gamma"][s],
+                                       ov["idx"][s], ov["n"][s]))
+    cache = np.concatenate(pages)
+    q = rng.standard_normal((G, d))
+    reps, t_dec = 0, 0.0
+    while t_dec < seconds and reps < reps_max:
+        t0 = time.perf_counter()
+        tok = pagefmt.unpack_tokens(d, b, m, cache, T // 128, 0, 0, T, 1)
+        tk = dict(idx=tok["kidx"], n=tok["nk"].astype(np.float64), sigma=tok["sigma"],
+                  gamma=tok["gamma"].astype(np.float64))
+        tv = dict(idx=tok["vidx"], n=tok["nv"].astype(np.float64))
+        for h in range(G):
+            odec.attend_route_a(q[h], tk, tv, p.Pi, p.S, p.cb_k, p.cb_v)
+        t_dec += time.perf_counter() - t0
+        reps += 1
+    gbs = reps * T * bpt(d, b, m) / t_dec / 1e9
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    desc = (f"oracle decode of 1 KV head x {T} tokens ({T // 128} packed pages) for {G} query heads, "
+            f"{reps} reps in {t_dec:.1f} s; oracle quantize of {T} K+V vectors in {t_quant:.2f} s")
+    return gbs, T / t_quant / 1e6, threads, desc
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    sample_s = 2.0
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, seconds=sample_s / 4, reps_max=1)
+    vals, t_all = [], time.perf_counter()
+    for _ in range(args.steps):
+        gbs, mtok, threads, desc = cpu_oracle_sample(w, seconds=sample_s)
+        vals.append(gbs)
+    elapsed = time.perf_counter() - t_all
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "quantize_mtok_s": mtok,
+            "config": {"workload": w.name, "batch": w.batch, "kv_heads": w.kv_heads, "q_heads": w.q_heads,
+                       "tokens": w.tokens, "head_dim": w.d, "bits": w.b, "decode_steps": w.decode_steps,
+                       "sample": "bounded CPU sample per step (see cpu_baseline)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import kv_cache_vector_19_b300 as tq
+    from kv_cache_vector_19_b300 import workloads
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(w)             # before any GPU work
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    wl = workloads.preset(w.name, seed=w.seed + rank)
+    data = workloads.generate(wl)
+    B, H, Hq, T, d, S = wl.batch, wl.kv_heads, wl.q_heads, wl.tokens, wl.d, wl.decode_steps
+    appends = S > 1
+    maxT = wl.max_tokens
+    dev = torch.device("cuda", local)
+
+    # pinned host copies (end-to-end leg) and device-resident copies (kernel leg)
+    h_k, h_v, h_q = data["k"].pin_memory(), data["v"].pin_memory(), data["q"].pin_memory()
+    k, v, q = h_k.to(dev), h_v.to(dev), h_q.to(dev)
+    if appends:
+        h_kn, h_vn = data["k_new"].pin_memory(), data["v_new"].pin_memory()
+        kn, vn = h_kn.to(dev), h_vn.to(dev)
+    del data
+
+    ctx = tq.Context(d, wl.b, seed=wl.seed, device=local)
+    cache = ctx.alloc_cache(B, H, maxT)
+    ws = ctx.alloc_workspace(B, Hq, H, maxT)
+    out = torch.empty(S, B, Hq, d, device=dev)
+    h_out = torch.empty(S, B, Hq, d).pin_memory()
+    zero = torch.zeros(B, dtype=torch.int32, device=dev)
+    pos = torch.tensor([[T + s] * B for s in range(S)], dtype=torch.int32, device=dev)
+    lens = pos + 1 if appends else torch.full((1, B), T, dtype=torch.int32, device=dev)
+
+    tev = lambda: torch.cuda.Event(enable_timing=True)
+    xev = lambda: torch.cuda.Event(enable_timing=True, external=True)
+    call_ev = [(xev(), xev()) for _ in range(S)]
+
+    def prefill(copies):
+        if copies:
+            k.copy_(h_k, non_blocking=True)
+            v.copy_(h_v, non_blocking=True)
+        ctx.quantize_kv(k, v, zero, cache, maxT)
+
+    def decode_phase(copies, events):
+        for s in range(S):
+            if copies:
+                q[s].copy_(h_q[s], non_blocking=True)
+                if appends:
+                    kn[s].copy_(h_kn[s], non_blocking=True)
+                    vn[s].copy_(h_vn[s], non_blocking=True)
+            if appends:
+                ctx.quantize_kv(kn[s], vn[s], pos[s], cache, maxT)
+            if events:
+                call_ev[s][0].record()
+            ctx.attn_decode(q[s], cache, lens[s], H, maxT, out[s], ws)
+            if events:
+                call_ev[s][1].record()
+            if copies:
+                h_out[s].copy_(out[s], non_blocking=True)
+
+    # the decode phase is launch-bound from Python, so each variant is one CUDA graph
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        prefill(False)
+        decode_phase(False, False)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    g_dec, g_e2e = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_dec):
+        decode_phase(False, True)
+    with torch.cuda.graph(g_e2e):
+        decode_phase(True, False)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    e_q0, e_q1, e_d1 = tev(), tev(), tev()
+
+    def step():
+        e_q0.record()
+        prefill(False)
+        e_q1.record()
+        g_dec.replay()
+        e_d1.record()
+
+    for _ in range(args.warmup):
+        step()
+    st = ctx.device_status()
+    if st != tq.TQ_OK:
+        raise SystemExit(f"device status after warm-up: {tq.tq_status_string(st)}")
+
+    q_ms, dphase_ms, dcall_ms = [], [], []
+    barrier()
+    t_start, t_end = tev(), tev()
+    with ClockSampler(local) as clk:
+        t_start.record()
+        for _ in range(args.steps):
+            step()
+            torch.cuda.synchronize()     # read this step's events; a step is several ms
+            q_ms.append(e_q0.elapsed_time(e_q1))
+            dphase_ms.append(e_q1.elapsed_time(e_d1))
+            dcall_ms.extend(a.elapsed_time(b) for a, b in call_ev)
+        t_end.record()
+        barrier()
+    total_ms = t_start.elapsed_time(t_end)
+
+    # end-to-end leg: the step's inputs come from pinned host memory and its outputs are
+    # read back, inside the timed region
+    e2e_steps = max(1, min(args.steps, 5))
+    prefill(True)
+    g_e2e.replay()
+    barrier()
+    e0, e1, e2 = tev(), tev(), tev()
+    e2e_q, e2e_d = [], []
+    for _ in range(e2e_steps):
+        e0.record()
+        prefill(True)
+        e1.record()
+        g_e2e.replay()
+        e2.record()
+        torch.cuda.synchronize()
+        e2e_q.append(e0.elapsed_time(e1))
+        e2e_d.append(e1.elapsed_time(e2))
+    barrier()
+    st = ctx.device_status()
+    if st != tq.TQ_OK:
+        raise SystemExit(f"device status after timing: {tq.tq_status_string(st)}")
+
+    per_token = bpt(d, wl.b, wl.m)
+    seq = [int(x) for x in lens[:, 0].tolist()]
+    dec_bytes = sum(B * H * n * per_token + 2 * B * Hq * d * 4 for n in seq)
+    per_launch_bytes = dec_bytes / S
+    mean = lambda xs: sum(xs) / len(xs)
+    t_dphase, t_q, t_call = mean(dphase_ms), mean(q_ms), mean(dcall_ms)
+    t_e2e_d, t_e2e_q = mean(e2e_d), mean(e2e_q)
+    if world > 1:
+        t = torch.tensor([t_dphase, t_q, t_call, total_ms, t_e2e_d, t_e2e_q], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_dphase, t_q, t_call, total_ms, t_e2e_d, t_e2e_q = t.tolist()
+    value = world * dec_bytes / (t_dphase * 1e-3) / 1e9
+    peak, peak_kind = read_peaks()
+    achieved = per_launch_bytes / (t_call * 1e-3) / 1e9
+    h2d = (h_k.numel() + h_v.numel()) * 2 + h_q.numel() * 4 + ((h_kn.numel() + h_vn.numel()) * 2 if appends else 0)
+    d2h = h_out.numel() * 4
+    launches_per_step = tq.binding.QUANTIZE_LAUNCHES * (1 + (S if appends else 0)) + tq.binding.DECODE_LAUNCHES * S
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded bf16 K/V, fp32 queries; no model weights)",
+        "config": {"workload": f"{wl.name}: batch {B}, {H} KV / {Hq} query heads, head_dim {d}, b={wl.b}, "
+                               f"{T} prefill tokens + {S} decode step(s)",
+                   "batch": B, "kv_heads": H, "q_heads": Hq, "tokens": T, "head_dim": d, "bits": wl.b,
+                   "decode_steps": S, "parallelism": f"replicas x{world} (independent sequences per GPU)",
+                   "l2": "inputs larger than L2 (compressed cache and bf16 K/V are each > 126 MB)"},
+        "quantize_mtok_s": world * B * T / (t_q * 1e-3) / 1e6,
+        "quantize_ms": t_q,
+        "decode_us_per_step": t_dphase / S * 1e3,
+        "decode_call_us": t_call * 1e3,
+        "roofline": {"bound": "hbm", "kernel": "tq_attn_decode", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": DECODE_TRAFFIC_BYTES, "algorithmic_bytes_per_launch": per_launch_bytes},
+        "e2e": {"value": world * dec_bytes / (t_e2e_d * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": t_e2e_q + t_e2e_d,
+                "quantize_mtok_s": world * B * T / (t_e2e_q * 1e-3) / 1e6},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clk.summary(),
+    }
+    if cpu is not None:
+        gbs, mtok, threads, desc = cpu
+        line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+                                "quantize_mtok_s": mtok}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    del g_dec, g_e2e
+    ctx.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_sweep(args):
+    """Throughput per (d, b) point of the bit/dim sweep (1 KV head, 65,536 tokens, 16 queries)."""
+    import torch
+
+    import kv_cache_vector_19_b300 as tq
+    from kv_cache_vector_19_b300 import workloads
+
+    for d in (64, 128, 256):
+        for b in (2, 3, 4, 5):
+            w = workloads.sweep_point(d, b)
+            data = workloads.generate(w)
+            T, nq = w.tokens, w.extra["n_queries"]
+            ctx = tq.Context(d, b, seed=w.seed)
+            cache = ctx.alloc_cache(1, 1, T)
+            ws = ctx.alloc_workspace(1, nq, 1, T)
+            k, v = data["k"].cuda(), data["v"].cuda()
+            q = data["q"][0].cuda().reshape(1, nq, d).contiguous()
+            out = torch.empty_like(q)
+            zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+            lens = torch.full((1,), T, dtype=torch.int32, device="cuda")
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            for _ in range(args.warmup):
+                ctx.quantize_kv(k, v, zero, cache, T)
+                ctx.attn_decode(q, cache, lens, 1, T, out, ws)
+            torch.cuda.synchronize()
+            e[0].record()
+            for _ in range(args.steps):
+                ctx.quantize_kv(k, v, zero, cache, T)
+            e[1].record()
+            for _ in range(args.steps):
+                ctx.attn_decode(q, cache, lens, 1, T, out, ws)
+            e[2].record()
+            torch.cuda.synchronize()
+            tq_ms = e[0].elapsed_time(e[1]) / args.steps
+            td_ms = e[1].elapsed_time(e[2]) / args.steps
+            nbytes = T * bpt(d, b, d)
+            print(json.dumps({"sweep_point": f"d{d}_b{b}", "head_dim": d, "bits": b, "tokens": T,
+                              "queries": nq, "quantize_mtok_s": T / tq_ms / 1e3, "decode_us": td_ms * 1e3,
+                              "decode_gbs": nbytes / td_ms / 1e6, "compressed_bytes": nbytes,
+                              "bytes_per_token": bpt(d, b, d), "compression_vs_bf16": 4 * d / bpt(d, b, d)}),
+                  flush=True)
+            ctx.close()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="longctx", choices=["longctx", "llama8b", "llama70b", "tiny"])
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and not args.sweep:
+        args.warmup = 3
+    from kv_cache_vector_19_b300 import workloads
+    w = workloads.preset(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    if args.sweep:
+        return run_sweep(args)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

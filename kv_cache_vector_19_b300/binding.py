@@ -1,0 +1,256 @@
+"""ctypes binding of ``libtq.so``: the same entry points as ``include/tq.h``.
+
+Argument marshalling only.  Every step of the quantize / decode path runs in the library's
+CUDA kernels; PyTorch is used here for nothing but device memory and the current stream.
+If the shared library cannot be built or loaded, every call raises: there is no fallback.
+"""
+import ctypes
+import os
+import re
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+HEADER = os.path.join(ROOT, "include", "tq.h")
+LIB_PATH = os.path.join(PKG, "libtq.so")
+
+TQ_OK = 0
+TQ_EINVAL = -1
+TQ_EUNSUPPORTED = -2
+TQ_ECUDA = -3
+TQ_ETIMEOUT = -4
+TQ_EBOUNDS = -5
+TQ_ENOMEM = -6
+TQ_ENOTCONV = -7
+PAGE_TOKENS = 128
+# kernels one call launches (the benchmark reports launch counts from these)
+QUANTIZE_LAUNCHES = 1
+DECODE_LAUNCHES = 3
+
+_lock = threading.Lock()
+_lib = None
+
+_c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+_dp = ctypes.POINTER(ctypes.c_double)
+
+# name -> (restype, argtypes)
+_SIGS = {
+    "tq_make_codebook": (_c_int, [_c_int, _c_int, _dp, _dp]),
+    "tq_make_rotation": (_c_int, [_c_int, ctypes.c_uint64, _dp]),
+    "tq_make_projection": (_c_int, [_c_int, _c_int, ctypes.c_uint64, _dp]),
+    "tq_ctx_create": (_c_int, [_c_int, _c_int, _c_int, ctypes.c_uint64, _c_int, ctypes.POINTER(_vp)]),
+    "tq_ctx_destroy": (None, [_vp]),
+    "tq_page_bytes": (_c_size, [_vp]),
+    "tq_cache_bytes": (_c_size, [_vp, _c_int, _c_int, _c_int]),
+    "tq_ctx_get_constants": (_c_int, [_vp, _dp, _dp, _dp, _dp, _dp, _dp]),
+    "tq_quantize_kv": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp]),
+    "tq_decode_workspace_bytes": (_c_size, [_vp, _c_int, _c_int, _c_int, _c_int]),
+    "tq_attn_decode": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp,
+                                _c_size, _vp]),
+    "tq_get_device_status": (_c_int, [_vp, _vp]),
+    "tq_status_string": (ctypes.c_char_p, [_c_int]),
+}
+
+
+class TQError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status} ({status_string(status)})")
+
+
+def header_functions():
+    """Names of the functions ``include/tq.h`` declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_\w+)\s*\(", text)))
+
+
+def lib():
+    """Loads libtq.so once (building it in-tree with nvcc first if it is missing or older
+    than its sources).  Raises if that fails."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            from . import build as _build
+            if not _build.up_to_date():
+                _build.build()
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(status):
+    return lib().tq_status_string(int(status)).decode()
+
+
+def _check(fn, rc):
+    if rc != TQ_OK:
+        raise TQError(fn, rc)
+
+
+def _ptr(t):
+    """Device (or host) address of a tensor, or None."""
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ---- host-only set-up ------------------------------------------------------------------
+
+def tq_make_codebook(d, levels):
+    """(centroids [levels], boundaries [levels-1]) as lists of floats (fp64)."""
+    c = (ctypes.c_double * levels)()
+    t = (ctypes.c_double * max(levels - 1, 1))()
+    _check("tq_make_codebook", lib().tq_make_codebook(d, levels, c, t))
+    return list(c), list(t)[:levels - 1]
+
+
+def tq_make_rotation(d, seed):
+    """Pi as a flat row-major list of d*d floats."""
+    buf = (ctypes.c_double * (d * d))()
+    _check("tq_make_rotation", lib().tq_make_rotation(d, ctypes.c_uint64(seed), buf))
+    return list(buf)
+
+
+def tq_make_projection(m, d, seed):
+    """S as a flat row-major list of m*d floats."""
+    buf = (ctypes.c_double * (m * d))()
+    _check("tq_make_projection", lib().tq_make_projection(m, d, ctypes.c_uint64(seed), buf))
+    return list(buf)
+
+
+# ---- raw C-ABI wrappers (pointers are ints or ctypes values) -------------------------------
+
+def tq_ctx_create(d, bits, m, seed, device):
+    out = ctypes.c_void_p()
+    _check("tq_ctx_create", lib().tq_ctx_create(d, bits, m, ctypes.c_uint64(seed), device, ctypes.byref(out)))
+    return out
+
+
+def tq_ctx_destroy(ctx):
+    lib().tq_ctx_destroy(ctx)
+
+
+def tq_page_bytes(ctx):
+    return lib().tq_page_bytes(ctx)
+
+
+def tq_cache_bytes(ctx, batch, kv_heads, max_tokens):
+    return lib().tq_cache_bytes(ctx, batch, kv_heads, max_tokens)
+
+
+def tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens):
+    return lib().tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens)
+
+
+def tq_quantize_kv(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream):
+    return lib().tq_quantize_kv(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream)
+
+
+def tq_attn_decode(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
+                   workspace, workspace_bytes, stream):
+    return lib().tq_attn_decode(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out,
+                                logits_out, workspace, workspace_bytes, stream)
+
+
+def tq_get_device_status(ctx, stream):
+    return lib().tq_get_device_status(ctx, stream)
+
+
+def tq_status_string(status):
+    return status_string(status)
+
+
+def tq_ctx_get_constants(ctx, d, bits, m):
+    """dict(pi, s, ck, tk, cv, tv) of flat fp64 lists (the context's host copies)."""
+    lk, lv = 2 ** (bits - 1), 2 ** bits
+    bufs = dict(pi=(ctypes.c_double * (d * d))(), s=(ctypes.c_double * (m * d))(),
+                ck=(ctypes.c_double * lk)(), tk=(ctypes.c_double * (lk - 1))(),
+                cv=(ctypes.c_double * lv)(), tv=(ctypes.c_double * (lv - 1))())
+    _check("tq_ctx_get_constants", lib().tq_ctx_get_constants(ctx, bufs["pi"], bufs["s"], bufs["ck"], bufs["tk"],
+                                                              bufs["cv"], bufs["tv"]))
+    return {k: list(v) for k, v in bufs.items()}
+
+
+# ---- tensor-level convenience (still only marshalling) --------------------------------------
+
+class Context:
+    """One (d, bits, m, seed) context on one CUDA device; wraps the C-ABI calls for torch
+    tensors.  Every method is asynchronous on the given (or current) stream."""
+
+    def __init__(self, d, bits, m=None, seed=0, device=0):
+        self.d, self.bits, self.m, self.seed, self.device = d, bits, d if m is None else m, seed, device
+        self._ctx = tq_ctx_create(d, bits, self.m, seed, device)
+
+    def close(self):
+        if self._ctx:
+            tq_ctx_destroy(self._ctx)
+            self._ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._ctx
+
+    @property
+    def page_bytes(self):
+        return tq_page_bytes(self._ctx)
+
+    def cache_bytes(self, batch, kv_heads, max_tokens):
+        return tq_cache_bytes(self._ctx, batch, kv_heads, max_tokens)
+
+    def workspace_bytes(self, batch, q_heads, kv_heads, max_tokens):
+        return tq_decode_workspace_bytes(self._ctx, batch, q_heads, kv_heads, max_tokens)
+
+    def alloc_cache(self, batch, kv_heads, max_tokens):
+        import torch
+        n = self.cache_bytes(batch, kv_heads, max_tokens)
+        if n == 0:
+            raise TQError("tq_cache_bytes", TQ_EINVAL)
+        return torch.empty(n, dtype=torch.uint8, device=f"cuda:{self.device}")
+
+    def alloc_workspace(self, batch, q_heads, kv_heads, max_tokens):
+        import torch
+        n = self.workspace_bytes(batch, q_heads, kv_heads, max_tokens)
+        if n == 0:
+            raise TQError("tq_decode_workspace_bytes", TQ_EINVAL)
+        return torch.empty(n, dtype=torch.uint8, device=f"cuda:{self.device}")
+
+    def quantize_kv(self, k, v, start_pos, cache, max_tokens, stream=None):
+        """k, v: bf16 [B, Hkv, n_tokens, d] contiguous; start_pos: int32 [B] on the device."""
+        B, H, N, d = k.shape
+        rc = tq_quantize_kv(self._ctx, _ptr(k), _ptr(v), B, H, N, _ptr(start_pos), _ptr(cache), max_tokens,
+                            _stream_handle(stream))
+        _check("tq_quantize_kv", rc)
+
+    def attn_decode(self, q, cache, seq_lens, kv_heads, max_tokens, out, workspace, logits=None, stream=None):
+        """q, out: fp32 [B, Hq, d]; seq_lens: int32 [B] on the device; logits: None or
+        fp32 [B, Hq, max_tokens]."""
+        B, Hq, d = q.shape
+        rc = tq_attn_decode(self._ctx, _ptr(q), B, Hq, kv_heads, _ptr(cache), _ptr(seq_lens), max_tokens,
+                            _ptr(out), _ptr(logits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            _stream_handle(stream))
+        _check("tq_attn_decode", rc)
+
+    def device_status(self, stream=None):
+        """Synchronises the stream; returns (and clears) the sticky device status code."""
+        return tq_get_device_status(self._ctx, _stream_handle(stream))
+
+    def constants(self):
+        return tq_ctx_get_constants(self._ctx, self.d, self.bits, self.m)

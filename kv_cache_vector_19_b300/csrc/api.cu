@@ -102,6 +102,7 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
     if (rc == TQ_OK) rc = upload(c->tk, &c->d_tk);
     if (rc == TQ_OK) rc = upload(c->cv, &c->d_cv);
     if (rc == TQ_OK) rc = upload(c->tv, &c->d_tv);
+    if (rc == TQ_OK) rc = prepare_quantize_simt(c);
     if (rc == TQ_OK) {
       if (cudaMalloc(&c->d_status, sizeof(int)) != cudaSuccess ||
           cudaMemset(c->d_status, 0, sizeof(int)) != cudaSuccess)

@@ -274,12 +274,17 @@ constexpr size_t quant_smem_bytes() {
 }
 
 template <int D, int BITS>
+int prepare_q() {
+  return cudaFuncSetAttribute(quantize_simt_kernel<D, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)quant_smem_bytes<D>()) == cudaSuccess
+             ? TQ_OK
+             : TQ_ECUDA;
+}
+
+template <int D, int BITS>
 int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
              const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st) {
   constexpr size_t smem = quant_smem_bytes<D>();
-  if (cudaFuncSetAttribute(quantize_simt_kernel<D, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
-    return TQ_ECUDA;
   QArgs a;
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
@@ -303,6 +308,16 @@ int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_he
 
 }  // namespace
 }  // namespace tq
+
+int prepare_quantize_simt(const tq_ctx* c) {
+#define TQ_P(DD, BB) \
+  if (c->d == DD && c->bits == BB) return tq::prepare_q<DD, BB>();
+  TQ_P(64, 2) TQ_P(64, 3) TQ_P(64, 4) TQ_P(64, 5)
+  TQ_P(128, 2) TQ_P(128, 3) TQ_P(128, 4) TQ_P(128, 5)
+  TQ_P(256, 2) TQ_P(256, 3) TQ_P(256, 4) TQ_P(256, 5)
+#undef TQ_P
+  return TQ_EUNSUPPORTED;
+}
 
 int launch_quantize_simt(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads,
                          int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,

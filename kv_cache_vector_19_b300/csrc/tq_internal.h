@@ -49,6 +49,10 @@ struct tq_ctx {
   int* d_status = nullptr;  // sticky flags
 };
 
+// One-time per-context kernel attributes (dynamic shared memory limits), so that the
+// launchers themselves make no configuration calls and can be captured in CUDA graphs.
+int prepare_quantize_simt(const tq_ctx* ctx);
+
 // Kernel launchers (return TQ_OK or TQ_ECUDA).
 int launch_quantize_simt(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
                          int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,

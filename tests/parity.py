@@ -1,0 +1,139 @@
+"""Shared helpers of the GPU parity tests: run the library through its C ABI, run the
+oracle on the same seeded inputs, and compare them under the acceptance bars.
+
+Bars (from the method's acceptance statement):
+  * packing and indexing bit-exact (the oracle's own packer re-packs the GPU's codes into
+    identical page bytes);
+  * code + sign mismatch rate <= 1e-4, and every mismatch within a hair of a quantizer
+    boundary (|yhat - t_k| < 1e-3/sqrt(d), or |(S r)_i| < 1e-3 * gamma);
+  * logits within 2e-3 absolute of the oracle's logits on the GPU's own pages;
+  * decode outputs within 1e-2 relative L2 of the oracle's quantize + decode.
+"""
+import numpy as np
+import torch
+
+import kv_cache_vector_19_b300 as tq
+from oracle import decode as odec
+from oracle import pagefmt, params, quant
+
+MISMATCH_RATE = 1e-4
+LOGIT_ATOL = 2e-3
+OUT_REL_L2 = 1e-2
+
+
+class Run:
+    """A context plus device buffers for one workload shape."""
+
+    def __init__(self, d, b, batch, kv_heads, q_heads, max_tokens, seed=0):
+        self.d, self.b, self.m = d, b, d
+        self.batch, self.kv_heads, self.q_heads, self.max_tokens = batch, kv_heads, q_heads, max_tokens
+        self.ctx = tq.Context(d, b, seed=seed)
+        self.cache = self.ctx.alloc_cache(batch, kv_heads, max_tokens)
+        self.ws = self.ctx.alloc_workspace(batch, q_heads, kv_heads, max_tokens)
+        self.n_pages = (max_tokens + 127) // 128
+        self.p = params.make(d, b, seed=seed)
+
+    def quantize(self, k, v, start_pos):
+        start = torch.as_tensor(start_pos, dtype=torch.int32, device="cuda")
+        self.ctx.quantize_kv(k.cuda().contiguous(), v.cuda().contiguous(), start, self.cache, self.max_tokens)
+
+    def decode(self, q, seq_lens, logits=False):
+        qd = q.cuda().float().contiguous()
+        sl = torch.as_tensor(seq_lens, dtype=torch.int32, device="cuda")
+        out = torch.empty_like(qd)
+        lg = None
+        if logits:
+            lg = torch.full((self.batch, self.q_heads, self.max_tokens), float("nan"), device="cuda")
+        self.ctx.attn_decode(qd, self.cache, sl, self.kv_heads, self.max_tokens, out, self.ws, logits=lg)
+        return out, lg
+
+    def status(self):
+        return self.ctx.device_status()
+
+    def cache_np(self):
+        torch.cuda.synchronize()
+        return self.cache.cpu().numpy()
+
+    def tokens(self, cache_np, bb, h, n_tokens):
+        return pagefmt.unpack_tokens(self.d, self.b, self.m, cache_np, self.n_pages, bb, h, n_tokens,
+                                     self.kv_heads)
+
+
+def to64(x):
+    return x.double().numpy() if isinstance(x, torch.Tensor) else np.asarray(x, dtype=np.float64)
+
+
+def near_boundary(yhat, boundaries, d):
+    t = np.asarray(boundaries)
+    if len(t) == 0:
+        return np.zeros_like(yhat, dtype=bool)
+    dist = np.min(np.abs(yhat[..., None] - t), axis=-1)
+    return dist < 1e-3 / np.sqrt(d)
+
+
+def compare_sequence(run, X_k, X_v, got):
+    """Compares the GPU's unpacked tokens ``got`` for vectors X_k, X_v ([N, d] fp64) with
+    the oracle.  Returns dict(mismatches, total, bad (not near a boundary), max norm errors)."""
+    p = run.p
+    ok = quant.quantize_keys(X_k, p.Pi, p.S, p.cb_k)
+    ov = quant.quantize_values(X_v, p.Pi, p.cb_v)
+    kmis = got["kidx"] != ok["idx"]
+    vmis = got["vidx"] != ov["idx"]
+    bad = int(np.sum(kmis & ~near_boundary(ok["yhat"], p.cb_k[1], run.d)))
+    bad += int(np.sum(vmis & ~near_boundary(ov["yhat"], p.cb_v[1], run.d)))
+    # the QJL stage is judged on the GPU's own codes, so that one stage-1 flip near a
+    # boundary is not counted again as the sign flips it causes
+    sig, gam, z = quant.qjl_stage(X_k, got["kidx"], ok["n64"], p.Pi, p.S, p.cb_k[0])
+    smis = got["sigma"] != sig
+    bad += int(np.sum(smis & ~(np.abs(z) < 1e-3 * gam[:, None])))
+    mism = int(kmis.sum() + vmis.sum() + smis.sum())
+    total = kmis.size + vmis.size + smis.size
+    nz = ok["n64"] > 0
+    err_nk = np.max(np.abs(got["nk"] - ok["n64"])[nz] / ok["n64"][nz]) if nz.any() else 0.0
+    nzv = ov["n64"] > 0
+    err_nv = np.max(np.abs(got["nv"] - ov["n64"])[nzv] / ov["n64"][nzv]) if nzv.any() else 0.0
+    gz = gam > 0
+    err_g = np.max(np.abs(got["gamma"] - gam)[gz] / gam[gz]) if gz.any() else 0.0
+    return dict(mismatches=mism, total=total, bad=bad, err_nk=float(err_nk), err_nv=float(err_nv),
+                err_gamma=float(err_g), kmis=int(kmis.sum()), vmis=int(vmis.sum()), smis=int(smis.sum()),
+                oracle_k=ok, oracle_v=ov)
+
+
+def assert_quantize_ok(res, rate=MISMATCH_RATE):
+    assert res["bad"] == 0, res
+    assert res["mismatches"] <= rate * res["total"], (res["kmis"], res["vmis"], res["smis"], res["total"])
+    assert res["err_nk"] < 2e-6 and res["err_nv"] < 2e-6, (res["err_nk"], res["err_nv"])
+    assert res["err_gamma"] < 1e-4, res["err_gamma"]
+
+
+def repack_matches(run, cache_np, bb, h, page, got_page):
+    """The oracle's packer, fed the GPU's unpacked page, reproduces the GPU's bytes."""
+    pb = pagefmt.page_bytes(run.d, run.b, run.m)
+    base = ((bb * run.kv_heads) + h) * run.n_pages * pb + page * pb
+    raw = cache_np[base:base + pb]
+    again = pagefmt.pack_page(run.d, run.b, run.m, got_page["kidx"], got_page["sigma"], got_page["nk"],
+                              got_page["gamma"], got_page["vidx"], got_page["nv"])
+    return np.array_equal(raw, again)
+
+
+def oracle_logits_on_pages(run, q_row, tok):
+    """Route A logits / output of the oracle for one query over the GPU's own tokens."""
+    p = run.p
+    tk = dict(idx=tok["kidx"], n=tok["nk"].astype(np.float64), sigma=tok["sigma"],
+              gamma=tok["gamma"].astype(np.float64))
+    tv = dict(idx=tok["vidx"], n=tok["nv"].astype(np.float64))
+    out, lg = odec.attend_route_a(q_row, tk, tv, p.Pi, p.S, p.cb_k, p.cb_v)
+    return out, lg
+
+
+def oracle_end_to_end(run, q_row, ok, ov):
+    """Oracle quantize (its own codes) + decode for one query."""
+    p = run.p
+    tk = dict(idx=ok["idx"], n=ok["n"].astype(np.float64), sigma=ok["sigma"], gamma=ok["gamma"].astype(np.float64))
+    tv = dict(idx=ov["idx"], n=ov["n"].astype(np.float64))
+    return odec.attend_route_a(q_row, tk, tv, p.Pi, p.S, p.cb_k, p.cb_v)
+
+
+def rel_l2(a, b):
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / nb) if nb > 0 else float(np.linalg.norm(a))
