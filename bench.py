@@ -106,7 +106,6 @@ def cpu_oracle_sample(w, seconds=12.0, reps_max=1000):
     of one KV head) on a 1024-token sample of the workload, repeated for ~`seconds`.
     Returns (GB/s of compressed pages decoded, Mtokens/s quantized, threads, description)."""
     import numpy as np
-    from threadpoolctl import threadpool_info
 
     from oracle import decode as odec
     from oracle import pagefmt, params, quant
@@ -141,7 +140,11 @@ def cpu_oracle_sample(w, seconds=12.0, reps_max=1000):
         t_dec += time.perf_counter() - t0
         reps += 1
     gbs = reps * T * bpt(d, b, m) / t_dec / 1e9
-    threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except ImportError:   # BLAS pools default to one thread per host core
+        threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count())))
     desc = (f"oracle decode of 1 KV head x {T} tokens ({T // 128} packed pages) for {G} query heads, "
             f"{reps} reps in {t_dec:.1f} s; oracle quantize of {T} K+V vectors in {t_quant:.2f} s")
     return gbs, T / t_quant / 1e6, threads, desc

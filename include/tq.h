@@ -132,7 +132,8 @@ int tq_ctx_get_constants(const tq_ctx* ctx, double* pi, double* s, double* ck, d
  *   cache      device, tq_cache_bytes(ctx, batch, kv_heads, max_tokens) bytes, 256-byte
  *              aligned; only the slots written are modified.
  * If start_pos[b] < 0 or start_pos[b] + n_tokens > max_tokens, sequence b is skipped and
- * the sticky TQ_EBOUNDS flag is set.  Calls that write the same page must be ordered. */
+ * the sticky TQ_EBOUNDS flag is set.  Calls that write the same page must be ordered.
+ * n_tokens == 0 is a no-op that returns TQ_OK (k, v, start_pos and cache may then be NULL). */
 int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
                    int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
                    void* stream);

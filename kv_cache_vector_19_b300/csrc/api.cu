@@ -145,12 +145,13 @@ extern "C" int tq_ctx_get_constants(const tq_ctx* ctx, double* pi, double* s, do
 extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
                               int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
                               void* stream) {
-  if (!ctx || !k || !v || !start_pos || !cache) return TQ_EINVAL;
+  if (!ctx) return TQ_EINVAL;
   if (batch < 1 || kv_heads < 1 || n_tokens < 0 || max_tokens < 1) return TQ_EINVAL;
   if (batch > 65535 || kv_heads > 65535) return TQ_EINVAL;
   if (n_tokens > max_tokens) return TQ_EINVAL;
+  if (n_tokens == 0) return TQ_OK;   // nothing to read or write; k and v may be NULL
+  if (!k || !v || !start_pos || !cache) return TQ_EINVAL;
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(cache, 256) || !aligned(start_pos, 4)) return TQ_EINVAL;
-  if (n_tokens == 0) return TQ_OK;
   DeviceGuard guard(ctx->device);
   return launch_quantize_simt(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
 }
