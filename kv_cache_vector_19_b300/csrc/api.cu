@@ -7,6 +7,7 @@
 #include <new>
 #include <vector>
 
+#include "bitplane.h"
 #include "tq_internal.h"
 
 namespace {
@@ -25,12 +26,32 @@ int upload(const std::vector<double>& src, float** dst) {
   return TQ_OK;
 }
 
+// alpha_M = (1/L) sum_idx c[idx] prod_{q in M} (2 bit_q(idx) - 1) over the odd subsets M of
+// the code bits, listed by tq::mono_mask (bitplane.h).
+std::vector<double> plane_alphas(const std::vector<double>& book, int bits) {
+  const int L = 1 << bits, n = 1 << (bits - 1);
+  std::vector<double> al(n, 0.0);
+  for (int i = 0; i < n; ++i) {
+    const int mask = tq::mono_mask(i);
+    double acc = 0.0;
+    for (int idx = 0; idx < L; ++idx) {
+      double sgn = 1.0;
+      for (int q = 0; q < bits; ++q)
+        if ((mask >> q) & 1) sgn *= ((idx >> q) & 1) ? 1.0 : -1.0;
+      acc += book[idx] * sgn;
+    }
+    al[i] = acc / L;
+  }
+  return al;
+}
+
 void release(tq_ctx* c) {
   if (!c) return;
   int prev = -1;
   cudaGetDevice(&prev);
   cudaSetDevice(c->device);
-  float* bufs[] = {c->d_pi, c->d_pit, c->d_st, c->d_spt, c->d_ck, c->d_tk, c->d_cv, c->d_tv};
+  float* bufs[] = {c->d_pi, c->d_pit, c->d_st, c->d_spt, c->d_ck, c->d_tk, c->d_cv, c->d_tv, c->d_alpha_k,
+                   c->d_alpha_v};
   for (float* p : bufs)
     if (p) cudaFree(p);
   if (c->d_status) cudaFree(c->d_status);
@@ -102,7 +123,17 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
     if (rc == TQ_OK) rc = upload(c->tk, &c->d_tk);
     if (rc == TQ_OK) rc = upload(c->cv, &c->d_cv);
     if (rc == TQ_OK) rc = upload(c->tv, &c->d_tv);
+    if (rc == TQ_OK) {
+      std::vector<double> ak = plane_alphas(c->ck, bits - 1), av = plane_alphas(c->cv, bits);
+      for (double x : ak) c->asum_k += (float)x;
+      for (double x : av) c->asum_v += (float)x;
+      rc = upload(ak, &c->d_alpha_k);
+      if (rc == TQ_OK) rc = upload(av, &c->d_alpha_v);
+    }
+    if (rc == TQ_OK && cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+      rc = TQ_ECUDA;
     if (rc == TQ_OK) rc = prepare_quantize_simt(c);
+    if (rc == TQ_OK) rc = tq::prepare_decode_mma(c);
     if (rc == TQ_OK) {
       if (cudaMalloc(&c->d_status, sizeof(int)) != cudaSuccess ||
           cudaMemset(c->d_status, 0, sizeof(int)) != cudaSuccess)
@@ -159,6 +190,9 @@ extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, i
 extern "C" size_t tq_decode_workspace_bytes(const tq_ctx* ctx, int batch, int q_heads, int kv_heads,
                                             int max_tokens) {
   if (!ctx || batch < 1 || q_heads < 1 || kv_heads < 1 || max_tokens < 1) return 0;
+  tq::MmaPlan mp;
+  if (tq::plan_decode_mma(ctx, batch, q_heads, kv_heads, max_tokens, &mp))
+    return tq::decode_mma_workspace(ctx, mp, batch, q_heads, kv_heads);
   tq::SplitPlan sp = tq::plan_splits(batch, kv_heads, max_tokens);
   size_t rows = (size_t)batch * q_heads;
   size_t floats = rows * ctx->d * 2 + rows * sp.splits * (2 + ctx->d);
@@ -178,6 +212,10 @@ extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int 
     return TQ_EINVAL;
   if (workspace_bytes < tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens)) return TQ_ENOMEM;
   DeviceGuard guard(ctx->device);
+  tq::MmaPlan mp;
+  if (tq::plan_decode_mma(ctx, batch, q_heads, kv_heads, max_tokens, &mp))
+    return tq::launch_decode_mma(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
+                                 workspace, stream);
   return launch_decode_simt(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
                             workspace, stream);
 }

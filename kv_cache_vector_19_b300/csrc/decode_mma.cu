@@ -1,0 +1,180 @@
+// Launch plan, instantiations and the split-merge kernel of the tensor-core decode path.
+#include <cuda_runtime.h>
+
+#include "decode_mma.cuh"
+
+namespace tq {
+namespace dmma {
+namespace {
+
+// Merges the partial records of one (query head, batch) and rotates back: out = Pi^T o~ / l.
+template <int D>
+__global__ void __launch_bounds__(D) combine_kernel(const float* __restrict__ part, const float* __restrict__ pi,
+                                                    float* __restrict__ out, int q_heads, int kv_heads, int group,
+                                                    int pages_per_seq, int chunk, int slots, int grid) {
+  __shared__ float s_o[D];
+  __shared__ float s_w[512];
+  __shared__ float s_norm;
+  const int hq = blockIdx.x, b = blockIdx.y;
+  const size_t row = (size_t)b * q_heads + hq;
+  const int seq = b * kv_heads + hq / group, hh = hq % group;
+  const int first = (int)(((long)seq * pages_per_seq) / chunk);
+  const int last = min(grid - 1, (int)(((long)(seq + 1) * pages_per_seq - 1) / chunk));
+  const int n = last - first + 1;
+  const int j = threadIdx.x;
+  auto rec = [&](int s) { return part + (((size_t)seq * slots + s) * group + hh) * (2 + D); };
+  if (j == 0) {
+    float mx = -INFINITY;
+    for (int s = 0; s < n; ++s) mx = fmaxf(mx, rec(s)[0]);
+    float l = 0.f;
+    for (int s = 0; s < n; ++s) {
+      float m = rec(s)[0];
+      float w = (m == -INFINITY) ? 0.f : __expf(m - mx);
+      s_w[s] = w;
+      l += w * rec(s)[1];
+    }
+    s_norm = l > 0.f ? 1.f / l : 0.f;
+  }
+  __syncthreads();
+  float acc = 0.f;
+  for (int s = 0; s < n; ++s) {
+    float w = s_w[s];
+    if (w != 0.f) acc = fmaf(w, rec(s)[2 + j], acc);
+  }
+  s_o[j] = acc * s_norm;
+  __syncthreads();
+  float r = 0.f;
+#pragma unroll 8
+  for (int k = 0; k < D; ++k) r = fmaf(pi[(size_t)k * D + j], s_o[k], r);   // Pi[k][j] o~[k]
+  out[row * D + j] = r;
+}
+
+template <int D, int BITS, int NGRP>
+int prepare_one() {
+  using C = Cfg<D, BITS, NGRP>;
+  if constexpr (!C::SUPPORTED) {
+    return TQ_OK;
+  } else {
+    return cudaFuncSetAttribute(decode_mma_kernel<D, BITS, NGRP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM) == cudaSuccess
+               ? TQ_OK
+               : TQ_ECUDA;
+  }
+}
+
+template <int D, int BITS, int NGRP>
+bool plan_one(const tq_ctx* c, int batch, int kv_heads, int max_tokens, MmaPlan* p) {
+  using C = Cfg<D, BITS, NGRP>;
+  if constexpr (!C::SUPPORTED) {
+    return false;
+  } else {
+    const long pm = (max_tokens + 127) / 128;
+    const long total = (long)batch * kv_heads * pm;
+    if (total > 0x7fffffffL) return false;
+    long cap = (long)c->num_sms * C::MINB;
+    long grid = total < cap ? total : cap;
+    if (grid < 1) grid = 1;
+    long chunk = (total + grid - 1) / grid;
+    grid = (total + chunk - 1) / chunk;
+    p->pages_per_seq = (int)pm;
+    p->total_pages = (int)total;
+    p->chunk = (int)chunk;
+    p->grid = (int)grid;
+    p->slots = (int)((pm - 1) / chunk + 2);
+    return true;
+  }
+}
+
+template <int D, int BITS, int NGRP>
+int launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
+               const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws,
+               cudaStream_t st) {
+  using C = Cfg<D, BITS, NGRP>;
+  if constexpr (!C::SUPPORTED) {
+    return TQ_EUNSUPPORTED;
+  } else {
+    float* qr = static_cast<float*>(ws);
+    float* qs = qr + (size_t)batch * q_heads * D;
+    float* part = qs + (size_t)batch * q_heads * D;
+    launch_prologue(c, q, batch, q_heads, qr, qs, st);
+    Params a;
+    a.qr = qr;
+    a.qs = qs;
+    a.cache = static_cast<const uint8_t*>(cache);
+    a.seq_lens = seq_lens;
+    a.logits = logits;
+    a.part = part;
+    a.alpha_k = c->d_alpha_k;
+    a.alpha_v = c->d_alpha_v;
+    a.status = c->d_status;
+    a.asum_k = c->asum_k;
+    a.asum_v = c->asum_v;
+    a.batch = batch;
+    a.q_heads = q_heads;
+    a.kv_heads = kv_heads;
+    a.group = q_heads / kv_heads;
+    a.max_tokens = max_tokens;
+    a.pages_per_seq = pl.pages_per_seq;
+    a.chunk = pl.chunk;
+    a.slots = pl.slots;
+    a.total_pages = pl.total_pages;
+    decode_mma_kernel<D, BITS, NGRP><<<pl.grid, kThreads, C::SMEM, st>>>(a);
+    combine_kernel<D><<<dim3(q_heads, batch), D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
+                                                          pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
+    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
+  }
+}
+
+int ngrp_of(int group) { return group <= 4 ? 1 : group <= 8 ? 2 : group <= 16 ? 4 : 0; }
+
+}  // namespace
+}  // namespace dmma
+
+#define TQ_FOR_ALL(X)                                                                                     \
+  X(64, 2, 1) X(64, 2, 2) X(64, 2, 4) X(64, 3, 1) X(64, 3, 2) X(64, 3, 4) X(64, 4, 1) X(64, 4, 2)           \
+  X(64, 4, 4) X(64, 5, 1) X(64, 5, 2) X(64, 5, 4) X(128, 2, 1) X(128, 2, 2) X(128, 2, 4) X(128, 3, 1)        \
+  X(128, 3, 2) X(128, 3, 4) X(128, 4, 1) X(128, 4, 2) X(128, 4, 4) X(128, 5, 1) X(128, 5, 2) X(128, 5, 4)    \
+  X(256, 2, 1) X(256, 2, 2) X(256, 2, 4) X(256, 3, 1) X(256, 3, 2) X(256, 3, 4) X(256, 4, 1) X(256, 4, 2)    \
+  X(256, 4, 4) X(256, 5, 1) X(256, 5, 2) X(256, 5, 4)
+
+int prepare_decode_mma(const tq_ctx* c) {
+  int rc = TQ_OK;
+#define TQ_P(DD, BB, NG) \
+  if (rc == TQ_OK && c->d == DD && c->bits == BB) rc = dmma::prepare_one<DD, BB, NG>();
+  TQ_FOR_ALL(TQ_P)
+#undef TQ_P
+  return rc;
+}
+
+bool plan_decode_mma(const tq_ctx* c, int batch, int q_heads, int kv_heads, int max_tokens, MmaPlan* p) {
+  if (q_heads % kv_heads != 0) return false;
+  const int ng = dmma::ngrp_of(q_heads / kv_heads);
+#define TQ_PL(DD, BB, NG) \
+  if (c->d == DD && c->bits == BB && ng == NG) return dmma::plan_one<DD, BB, NG>(c, batch, kv_heads, max_tokens, p);
+  TQ_FOR_ALL(TQ_PL)
+#undef TQ_PL
+  return false;
+}
+
+int launch_decode_mma(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
+                      const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
+                      void* workspace, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int ng = dmma::ngrp_of(q_heads / kv_heads);
+#define TQ_L(DD, BB, NG)                                                                                    \
+  if (c->d == DD && c->bits == BB && ng == NG)                                                              \
+    return dmma::launch_one<DD, BB, NG>(c, pl, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, \
+                                        logits_out, workspace, st);
+  TQ_FOR_ALL(TQ_L)
+#undef TQ_L
+  return TQ_EUNSUPPORTED;
+}
+
+size_t decode_mma_workspace(const tq_ctx* c, const MmaPlan& pl, int batch, int q_heads, int kv_heads) {
+  const size_t rows = (size_t)batch * q_heads;
+  const size_t n_seq = (size_t)batch * kv_heads;
+  const size_t g = (size_t)(q_heads / kv_heads);
+  return (rows * c->d * 2 + n_seq * pl.slots * g * (2 + c->d)) * sizeof(float);
+}
+
+}  // namespace tq

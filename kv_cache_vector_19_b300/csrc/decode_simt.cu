@@ -310,6 +310,15 @@ int launch_d(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_hea
 }
 
 }  // namespace
+
+void launch_prologue(const tq_ctx* c, const float* q, int batch, int q_heads, float* qr, float* qs,
+                     cudaStream_t st) {
+  dim3 grid(q_heads, batch);
+  if (c->d == 64) prologue_kernel<64><<<grid, 64, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
+  if (c->d == 128) prologue_kernel<128><<<grid, 128, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
+  if (c->d == 256) prologue_kernel<256><<<grid, 256, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
+}
+
 }  // namespace tq
 
 int launch_decode_simt(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_heads,

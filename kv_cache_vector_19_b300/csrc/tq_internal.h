@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <vector>
 
+#include <cuda_runtime.h>
+
 #include "tq.h"
 
 namespace tq {
@@ -29,6 +31,12 @@ struct SplitPlan {
 };
 SplitPlan plan_splits(int batch, int kv_heads, int max_tokens);
 
+// Tensor-core decode plan: the call's (sequence, page) list cut into `grid` ranges of
+// `chunk` pages; every sequence has `slots` partial-record slots.
+struct MmaPlan {
+  int grid, chunk, slots, pages_per_seq, total_pages;
+};
+
 }  // namespace tq
 
 struct tq_ctx {
@@ -47,6 +55,11 @@ struct tq_ctx {
   float* d_cv = nullptr;    // [lv]
   float* d_tv = nullptr;    // [lv-1]
   int* d_status = nullptr;  // sticky flags
+  // bit-plane expansion of the books: c[idx] = 2 sum_M alpha_M x_M(idx) - sum_M alpha_M
+  float* d_alpha_k = nullptr;   // [2^(bits-2)]
+  float* d_alpha_v = nullptr;   // [2^(bits-1)]
+  float asum_k = 0.f, asum_v = 0.f;
+  int num_sms = 148;
 };
 
 // One-time per-context kernel attributes (dynamic shared memory limits), so that the
@@ -57,6 +70,18 @@ int prepare_quantize_simt(const tq_ctx* ctx);
 int launch_quantize_simt(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
                          int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
                          void* stream);
+namespace tq {
+int prepare_decode_mma(const tq_ctx* c);
+bool plan_decode_mma(const tq_ctx* c, int batch, int q_heads, int kv_heads, int max_tokens, MmaPlan* p);
+int launch_decode_mma(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
+                      const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
+                      void* workspace, void* stream);
+size_t decode_mma_workspace(const tq_ctx* c, const MmaPlan& pl, int batch, int q_heads, int kv_heads);
+// q~ = Pi q and q_s = S q for every (batch, query head), fp32.
+void launch_prologue(const tq_ctx* c, const float* q, int batch, int q_heads, float* qr, float* qs,
+                     cudaStream_t st);
+}  // namespace tq
+
 int launch_decode_simt(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
                        const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
                        float* logits_out, void* workspace, void* stream);
