@@ -134,6 +134,7 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
       rc = TQ_ECUDA;
     if (rc == TQ_OK) rc = prepare_quantize_simt(c);
     if (rc == TQ_OK) rc = tq::prepare_decode_mma(c);
+    if (rc == TQ_OK) rc = tq::prepare_decode_tc(c);
     if (rc == TQ_OK) {
       if (cudaMalloc(&c->d_status, sizeof(int)) != cudaSuccess ||
           cudaMemset(c->d_status, 0, sizeof(int)) != cudaSuccess)
@@ -213,9 +214,13 @@ extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int 
   if (workspace_bytes < tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens)) return TQ_ENOMEM;
   DeviceGuard guard(ctx->device);
   tq::MmaPlan mp;
-  if (tq::plan_decode_mma(ctx, batch, q_heads, kv_heads, max_tokens, &mp))
+  if (tq::plan_decode_mma(ctx, batch, q_heads, kv_heads, max_tokens, &mp)) {
+    if (tq::decode_tc_supported(ctx, q_heads, kv_heads))
+      return tq::launch_decode_tc(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
+                                  workspace, stream);
     return tq::launch_decode_mma(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
                                  workspace, stream);
+  }
   return launch_decode_simt(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
                             workspace, stream);
 }

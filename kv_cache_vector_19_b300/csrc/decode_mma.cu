@@ -5,7 +5,6 @@
 
 namespace tq {
 namespace dmma {
-namespace {
 
 // Merges the partial records of one (query head, batch) and rotates back: out = Pi^T o~ / l.
 template <int D>
@@ -48,6 +47,8 @@ __global__ void __launch_bounds__(D) combine_kernel(const float* __restrict__ pa
   for (int k = 0; k < D; ++k) r = fmaf(pi[(size_t)k * D + j], s_o[k], r);   // Pi[k][j] o~[k]
   out[row * D + j] = r;
 }
+
+namespace {
 
 template <int D, int BITS, int NGRP>
 int prepare_one() {
@@ -175,6 +176,111 @@ size_t decode_mma_workspace(const tq_ctx* c, const MmaPlan& pl, int batch, int q
   const size_t n_seq = (size_t)batch * kv_heads;
   const size_t g = (size_t)(q_heads / kv_heads);
   return (rows * c->d * 2 + n_seq * pl.slots * g * (2 + c->d)) * sizeof(float);
+}
+
+}  // namespace tq
+
+// ---------------------------------------------------------------- tcgen05 decode (d = 128)
+#include "decode_tc.cuh"
+
+namespace tq {
+namespace {
+
+template <int BITS, int GP>
+int tc_prepare_one() {
+  using C = dtc::Cfg<BITS, GP>;
+  if constexpr (!C::SUPPORTED) {
+    return TQ_OK;
+  } else {
+    return cudaFuncSetAttribute(dtc::decode_tc_kernel<BITS, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM) == cudaSuccess
+               ? TQ_OK
+               : TQ_ECUDA;
+  }
+}
+
+int tc_gp(int group) { return group <= 4 ? 4 : group <= 8 ? 8 : group <= 16 ? 16 : 0; }
+
+template <int BITS, int GP>
+int tc_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
+                  const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws,
+                  cudaStream_t st) {
+  using C = dtc::Cfg<BITS, GP>;
+  if constexpr (!C::SUPPORTED) {
+    return TQ_EUNSUPPORTED;
+  } else {
+    constexpr int D = 128;
+    float* qr = static_cast<float*>(ws);
+    float* qs = qr + (size_t)batch * q_heads * D;
+    float* part = qs + (size_t)batch * q_heads * D;
+    launch_prologue(c, q, batch, q_heads, qr, qs, st);
+    dmma::Params a;
+    a.qr = qr;
+    a.qs = qs;
+    a.cache = static_cast<const uint8_t*>(cache);
+    a.seq_lens = seq_lens;
+    a.logits = logits;
+    a.part = part;
+    a.alpha_k = c->d_alpha_k;
+    a.alpha_v = c->d_alpha_v;
+    a.status = c->d_status;
+    a.asum_k = c->asum_k;
+    a.asum_v = c->asum_v;
+    a.batch = batch;
+    a.q_heads = q_heads;
+    a.kv_heads = kv_heads;
+    a.group = q_heads / kv_heads;
+    a.max_tokens = max_tokens;
+    a.pages_per_seq = pl.pages_per_seq;
+    a.chunk = pl.chunk;
+    a.slots = pl.slots;
+    a.total_pages = pl.total_pages;
+    dtc::decode_tc_kernel<BITS, GP><<<pl.grid, dtc::kThreads, C::SMEM, st>>>(a);
+    dmma::combine_kernel<D><<<dim3(q_heads, batch), D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
+                                                                pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
+    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
+  }
+}
+
+}  // namespace
+
+bool decode_tc_supported(const tq_ctx* c, int q_heads, int kv_heads) {
+  if (c->d != 128 || q_heads % kv_heads != 0) return false;
+  // A tcgen05.mma of M = 128, K = 32 costs about the same for every N up to 64, so the
+  // tensor-memory kernel pays off only when a KV head carries many query heads; with up
+  // to 8 the mma.sync kernel is faster on B300.
+  if (q_heads / kv_heads <= 8) return false;
+  const int gp = tc_gp(q_heads / kv_heads);
+  if (gp == 0) return false;
+#define TQ_S(BB, GG) \
+  if (c->bits == BB && gp == GG) return dtc::Cfg<BB, GG>::SUPPORTED;
+  TQ_S(2, 4) TQ_S(2, 8) TQ_S(2, 16) TQ_S(3, 4) TQ_S(3, 8) TQ_S(3, 16)
+#undef TQ_S
+  return false;
+}
+
+int prepare_decode_tc(const tq_ctx* c) {
+  if (c->d != 128) return TQ_OK;
+  int rc = TQ_OK;
+#define TQ_P(BB, GG) \
+  if (rc == TQ_OK && c->bits == BB) rc = tc_prepare_one<BB, GG>();
+  TQ_P(2, 4) TQ_P(2, 8) TQ_P(2, 16) TQ_P(3, 4) TQ_P(3, 8) TQ_P(3, 16)
+#undef TQ_P
+  return rc;
+}
+
+int launch_decode_tc(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
+                     const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
+                     void* workspace, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int gp = tc_gp(q_heads / kv_heads);
+#define TQ_L(BB, GG)                                                                                         \
+  if (c->bits == BB && gp == GG)                                                                             \
+    return tc_launch_one<BB, GG>(c, pl, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out, \
+                                 workspace, st);
+  TQ_L(2, 4) TQ_L(2, 8) TQ_L(2, 16) TQ_L(3, 4) TQ_L(3, 8) TQ_L(3, 16)
+#undef TQ_L
+  return TQ_EUNSUPPORTED;
 }
 
 }  // namespace tq

@@ -34,6 +34,7 @@
 #include <cstdint>
 
 #include "bitplane.h"
+#include "dev_common.cuh"
 #include "layout.cuh"
 #include "tq_internal.h"
 
@@ -47,7 +48,6 @@ constexpr int kL2Ahead = 12;             // pages prefetched into L2 beyond the 
 constexpr float kTau = 3.0f;          // lazy-maximum threshold (natural-log units)
 constexpr float kSB = 2.0f;           // e4m3 range scale of the softmax weights (max 20*8*2 < 448)
 constexpr int kRowB = 144;            // bytes per row of the softmax-weight operand (padded)
-constexpr uint32_t kSpinLimit = 1u << 26;
 
 struct Params {
   const float* qr;          // [B][Hq][D]  Pi q
@@ -102,112 +102,7 @@ struct Cfg {
                                     OREGS <= 64 && SMEM <= 220 * 1024;
 };
 
-// ---------------------------------------------------------------- PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-// 1-D bulk copy global -> shared, completing on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait; false after kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Two floats -> two e4m3 bytes (round to nearest even, saturating): low byte = lo_val.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi_val, float lo_val) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi_val), "f"(lo_val));
-  return r;
-}
-
-// Two e4m3 bytes (low byte -> .x) back to floats.
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)v));
-  __half2 h = *reinterpret_cast<__half2*>(&h2);
-  return __half22float2(h);
-}
-
-// Word w with its bit k of every byte turned into four e4m3 operands beta_k + gamma_k*bit.
-template <int K>
-__device__ __forceinline__ uint32_t expand(uint32_t w) {
-  return (w & (0x01010101u << K)) | (e4m3_base(K) * 0x01010101u);
-}
-__device__ __forceinline__ uint32_t expand_rt(uint32_t w, uint32_t mask, uint32_t base) { return (w & mask) | base; }
-// expand<K> with K known only after unrolling (the switch folds away).
-__device__ __forceinline__ uint32_t expand_at(uint32_t w, int k) {
-  switch (k & 7) {
-    case 0: return expand<0>(w);
-    case 1: return expand<1>(w);
-    case 2: return expand<2>(w);
-    case 3: return expand<3>(w);
-    case 4: return expand<4>(w);
-    case 5: return expand<5>(w);
-    case 6: return expand<6>(w);
-    default: return expand<7>(w);
-  }
-}
-
-// Three-piece e4m3 split of v: v ~ hi + mid / 16 + lo / 256.  The later pieces are scaled
-// up by 2^4 and 2^8 so that they stay in the normal range; they sit in separate MMA
-// columns, and the epilogue applies the 2^-4 and 2^-8.
-__device__ __forceinline__ void split3(float v, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
-  hi = cvt_e4m3x2(0.f, v) & 0xFF;
-  float r1 = v - e4m3x2_to_f2(hi).x;
-  mid = cvt_e4m3x2(0.f, 16.f * r1) & 0xFF;
-  float r2 = r1 - 0.0625f * e4m3x2_to_f2(mid).x;
-  lo = cvt_e4m3x2(0.f, 256.f * r2) & 0xFF;
-}
-
-__device__ __forceinline__ float e4m3_val(uint32_t byte) { return e4m3x2_to_f2(byte).x; }
-__device__ __forceinline__ float split3_val(uint32_t hi, uint32_t mid, uint32_t lo) {
-  return e4m3_val(hi) + 0.0625f * e4m3_val(mid) + 0.00390625f * e4m3_val(lo);
-}
+using namespace dev;
 
 // ---------------------------------------------------------------- the kernel
 

@@ -77,6 +77,13 @@ int launch_decode_mma(const tq_ctx* c, const MmaPlan& pl, const float* q, int ba
                       const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
                       void* workspace, void* stream);
 size_t decode_mma_workspace(const tq_ctx* c, const MmaPlan& pl, int batch, int q_heads, int kv_heads);
+// tcgen05 decode (head_dim 128, b in {2, 3}, up to 16 query heads per KV head); same plan,
+// workspace and partial records as the mma.sync kernel.
+bool decode_tc_supported(const tq_ctx* c, int q_heads, int kv_heads);
+int prepare_decode_tc(const tq_ctx* c);
+int launch_decode_tc(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
+                     const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
+                     void* workspace, void* stream);
 // q~ = Pi q and q_s = S q for every (batch, query head), fp32.
 void launch_prologue(const tq_ctx* c, const float* q, int batch, int q_heads, float* qr, float* qs,
                      cudaStream_t st);
