@@ -81,7 +81,9 @@ enum {
   TQ_ETIMEOUT = -4,     /* a device-side bounded wait gave up (sticky device flag)       */
   TQ_EBOUNDS = -5,      /* device-side position / length beyond max_tokens (sticky flag) */
   TQ_ENOMEM = -6,       /* workspace too small, or a context allocation failed           */
-  TQ_ENOTCONV = -7      /* host codebook solver did not converge                        */
+  TQ_ENOTCONV = -7,     /* host codebook solver did not converge                        */
+  TQ_ESCRATCH = -8      /* request needs more than the static scratch of                */
+                        /* tq_attn_decode_noalloc (4 MiB)                               */
 };
 
 typedef struct tq_ctx tq_ctx;
@@ -157,6 +159,23 @@ size_t tq_decode_workspace_bytes(const tq_ctx* ctx, int batch, int q_heads, int 
 int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
                    const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
                    float* logits_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* tq_attn_decode without a caller-provided workspace, for callers that cannot allocate
+ * device memory at decode time (a serving loop whose memory pool is frozen after start-up,
+ * a plugin whose host framework forbids cudaMalloc during a request, code that must avoid
+ * the synchronisation an allocation can imply).  No counterpart on the pages: this is an
+ * interface convenience, the computation is exactly tq_attn_decode's.
+ * The scratch is one 4 MiB array in the library's device image (every GPU that loads the
+ * library holds it until the process exits); a request whose tq_decode_workspace_bytes
+ * exceeds 4 MiB returns TQ_ESCRATCH.  Nothing is allocated: no cudaMalloc, cudaFree or
+ * allocating library routine is called.  The scratch needs no initialisation, and it is
+ * shared by every call on a device and keeps the last call's contents, so calls that can
+ * overlap on the GPU (other streams, other threads) race: order them.  The first call on a
+ * device looks up the scratch address (cudaGetSymbolAddress) and must come before any
+ * stream capture.  Arguments and errors otherwise as tq_attn_decode. */
+int tq_attn_decode_noalloc(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                           const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
+                           float* logits_out, void* stream);
 
 /* Synchronises `stream`, then returns and clears the sticky device status: TQ_OK,
  * TQ_EBOUNDS or TQ_ETIMEOUT. */

@@ -22,6 +22,7 @@ TQ_ETIMEOUT = -4
 TQ_EBOUNDS = -5
 TQ_ENOMEM = -6
 TQ_ENOTCONV = -7
+TQ_ESCRATCH = -8
 PAGE_TOKENS = 128
 # kernels one call launches (the benchmark reports launch counts from these)
 QUANTIZE_LAUNCHES = 1
@@ -47,6 +48,7 @@ _SIGS = {
     "tq_decode_workspace_bytes": (_c_size, [_vp, _c_int, _c_int, _c_int, _c_int]),
     "tq_attn_decode": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp,
                                 _c_size, _vp]),
+    "tq_attn_decode_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp]),
     "tq_get_device_status": (_c_int, [_vp, _vp]),
     "tq_status_string": (ctypes.c_char_p, [_c_int]),
 }
@@ -162,6 +164,11 @@ def tq_attn_decode(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens
                    workspace, workspace_bytes, stream):
     return lib().tq_attn_decode(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out,
                                 logits_out, workspace, workspace_bytes, stream)
+
+
+def tq_attn_decode_noalloc(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out, stream):
+    return lib().tq_attn_decode_noalloc(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out,
+                                        logits_out, stream)
 
 
 def tq_get_device_status(ctx, stream):

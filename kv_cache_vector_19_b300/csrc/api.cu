@@ -248,6 +248,7 @@ extern "C" const char* tq_status_string(int status) {
     case TQ_EBOUNDS: return "device-side position or length beyond max_tokens";
     case TQ_ENOMEM: return "allocation failed or workspace too small";
     case TQ_ENOTCONV: return "codebook solver did not converge";
+    case TQ_ESCRATCH: return "request exceeds the 4 MiB static scratch of tq_attn_decode_noalloc";
     default: return "unknown status";
   }
 }

@@ -23,7 +23,7 @@ def test_library_exports_every_declared_function():
 
 def test_status_strings():
     assert tq.tq_status_string(0) == "ok"
-    for code in range(-7, 0):
+    for code in range(-8, 0):
         assert tq.tq_status_string(code) != "unknown status"
 
 
