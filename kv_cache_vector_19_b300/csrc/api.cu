@@ -45,6 +45,44 @@ std::vector<double> plane_alphas(const std::vector<double>& book, int bits) {
   return al;
 }
 
+uint16_t bf16_rne(float x) {   // round to nearest even (finite inputs)
+  uint32_t u;
+  std::memcpy(&u, &x, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+float bf16_to_f(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+// bf16 hi/lo operand blob of the tensor-core quantizer (head_dim 128): matrices M[n][k]
+// (Pi, then S' = S Pi^T) split as hi = bf16(M), lo = bf16(M - hi), each stored in the
+// no-swizzle K-major layout (8-row x 16-byte core matrices, 128 contiguous bytes each;
+// core (n/8, k/8) at (n/8) * 2048 + (k/8) * 128).
+std::vector<uint8_t> quantizer_blob(const std::vector<double>& pi, const std::vector<double>& spt_kmajor) {
+  const int d = 128;
+  std::vector<uint8_t> blob(4 * d * d * 2);
+  auto put = [&](int mat, int n, int k, uint16_t v) {
+    size_t off = (size_t)mat * d * d * 2 + (size_t)(n >> 3) * 2048 + (size_t)(k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2;
+    blob[off] = (uint8_t)(v & 0xFF);
+    blob[off + 1] = (uint8_t)(v >> 8);
+  };
+  for (int n = 0; n < d; ++n)
+    for (int k = 0; k < d; ++k) {
+      const float p = (float)pi[(size_t)n * d + k];   // rotation: y_n = sum_k Pi[n][k] x_k
+      const float s = (float)spt_kmajor[(size_t)n * d + k];   // projection: z_n = sum_k S'[n][k] r_k
+      const uint16_t ph = bf16_rne(p), sh = bf16_rne(s);
+      put(0, n, k, ph);
+      put(1, n, k, bf16_rne(p - bf16_to_f(ph)));
+      put(2, n, k, sh);
+      put(3, n, k, bf16_rne(s - bf16_to_f(sh)));
+    }
+  return blob;
+}
+
 void release(tq_ctx* c) {
   if (!c) return;
   int prev = -1;
@@ -55,6 +93,7 @@ void release(tq_ctx* c) {
   for (float* p : bufs)
     if (p) cudaFree(p);
   if (c->d_status) cudaFree(c->d_status);
+  if (c->d_qblob) cudaFree(c->d_qblob);
   if (prev >= 0) cudaSetDevice(prev);
   delete c;
 }
@@ -135,6 +174,16 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
     if (rc == TQ_OK) rc = prepare_quantize_simt(c);
     if (rc == TQ_OK) rc = tq::prepare_decode_mma(c);
     if (rc == TQ_OK) rc = tq::prepare_decode_tc(c);
+    if (rc == TQ_OK && d == 128) {
+      std::vector<double> sp((size_t)m * d);   // S'[i][j] row-major
+      for (int i = 0; i < m; ++i)
+        for (int j = 0; j < d; ++j) sp[(size_t)i * d + j] = spt[(size_t)j * m + i];
+      std::vector<uint8_t> blob = quantizer_blob(c->pi, sp);
+      if (cudaMalloc(reinterpret_cast<void**>(&c->d_qblob), blob.size()) != cudaSuccess ||
+          cudaMemcpy(c->d_qblob, blob.data(), blob.size(), cudaMemcpyHostToDevice) != cudaSuccess)
+        rc = TQ_ENOMEM;
+      if (rc == TQ_OK) rc = tq::prepare_quantize_tc(c);
+    }
     if (rc == TQ_OK) {
       if (cudaMalloc(&c->d_status, sizeof(int)) != cudaSuccess ||
           cudaMemset(c->d_status, 0, sizeof(int)) != cudaSuccess)
@@ -185,6 +234,8 @@ extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, i
   if (!k || !v || !start_pos || !cache) return TQ_EINVAL;
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(cache, 256) || !aligned(start_pos, 4)) return TQ_EINVAL;
   DeviceGuard guard(ctx->device);
+  if (ctx->d == 128)
+    return tq::launch_quantize_tc(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
   return launch_quantize_simt(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
 }
 

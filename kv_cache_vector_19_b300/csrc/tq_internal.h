@@ -60,11 +60,19 @@ struct tq_ctx {
   float* d_alpha_v = nullptr;   // [2^(bits-1)]
   float asum_k = 0.f, asum_v = 0.f;
   int num_sms = 148;
+  // head_dim 128: bf16 B operands of the tensor-core quantizer, no-swizzle K-major layout:
+  // Pi hi, Pi lo, S' hi, S' lo (each 128 x 128, 32 KB)
+  uint8_t* d_qblob = nullptr;
 };
 
 // One-time per-context kernel attributes (dynamic shared memory limits), so that the
 // launchers themselves make no configuration calls and can be captured in CUDA graphs.
 int prepare_quantize_simt(const tq_ctx* ctx);
+namespace tq {
+int prepare_quantize_tc(const tq_ctx* c);
+int launch_quantize_tc(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
+                       const int32_t* start_pos, void* cache, int max_tokens, void* stream);
+}  // namespace tq
 
 // Kernel launchers (return TQ_OK or TQ_ECUDA).
 int launch_quantize_simt(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
