@@ -88,6 +88,17 @@ enum {
 
 typedef struct tq_ctx tq_ctx;
 
+/* Decode kernels (tq_ctx_set_decode_path).  All compute the same attention; they differ in
+ * speed and in the configurations they serve. */
+enum {
+  TQ_DECODE_AUTO = 0, /* fastest kernel that serves the call (the default)                */
+  TQ_DECODE_SIMT = 1, /* CUDA cores: every d, bits and group size                          */
+  TQ_DECODE_MMA = 2,  /* fp8 mma.sync over bit planes: d in {64,128,256}; how many query   */
+                      /* heads per kv head it takes shrinks as d and bits grow (registers) */
+  TQ_DECODE_TC = 3    /* tcgen05 over bit planes, operands in tensor memory: d == 128,     */
+                      /* bits in {2,3}, group size <= 16                                   */
+};
+
 /* ---- host-only set-up (no GPU needed) ------------------------------------------- */
 
 /* Lloyd-Max codebook for one coordinate of a uniform unit vector in R^d ([BLOG] 1.2,
@@ -123,6 +134,13 @@ size_t tq_cache_bytes(const tq_ctx* ctx, int batch, int kv_heads, int max_tokens
  * implementation. */
 int tq_ctx_get_constants(const tq_ctx* ctx, double* pi, double* s, double* ck, double* tk,
                          double* cv, double* tv);
+
+/* Selects the decode kernel of this context (TQ_DECODE_*).  Returns TQ_EINVAL for an
+ * unknown value and TQ_EUNSUPPORTED if the kernel cannot serve this context's d and bits;
+ * a group size the kernel cannot serve makes tq_attn_decode return TQ_EUNSUPPORTED.  The
+ * workspace size depends on the choice, so query tq_decode_workspace_bytes after it.  Not
+ * synchronised with decode calls: set it before the context is shared. */
+int tq_ctx_set_decode_path(tq_ctx* ctx, int path);
 
 /* ---- hot path ------------------------------------------------------------------- */
 

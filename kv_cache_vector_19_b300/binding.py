@@ -23,6 +23,8 @@ TQ_EBOUNDS = -5
 TQ_ENOMEM = -6
 TQ_ENOTCONV = -7
 TQ_ESCRATCH = -8
+TQ_DECODE_AUTO, TQ_DECODE_SIMT, TQ_DECODE_MMA, TQ_DECODE_TC = 0, 1, 2, 3
+DECODE_PATHS = {"auto": TQ_DECODE_AUTO, "simt": TQ_DECODE_SIMT, "mma": TQ_DECODE_MMA, "tc": TQ_DECODE_TC}
 PAGE_TOKENS = 128
 # kernels one call launches (the benchmark reports launch counts from these)
 QUANTIZE_LAUNCHES = 1
@@ -44,6 +46,7 @@ _SIGS = {
     "tq_page_bytes": (_c_size, [_vp]),
     "tq_cache_bytes": (_c_size, [_vp, _c_int, _c_int, _c_int]),
     "tq_ctx_get_constants": (_c_int, [_vp, _dp, _dp, _dp, _dp, _dp, _dp]),
+    "tq_ctx_set_decode_path": (_c_int, [_vp, _c_int]),
     "tq_quantize_kv": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp]),
     "tq_decode_workspace_bytes": (_c_size, [_vp, _c_int, _c_int, _c_int, _c_int]),
     "tq_attn_decode": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp,
@@ -196,9 +199,17 @@ class Context:
     """One (d, bits, m, seed) context on one CUDA device; wraps the C-ABI calls for torch
     tensors.  Every method is asynchronous on the given (or current) stream."""
 
-    def __init__(self, d, bits, m=None, seed=0, device=0):
+    def __init__(self, d, bits, m=None, seed=0, device=0, decode_path="auto"):
         self.d, self.bits, self.m, self.seed, self.device = d, bits, d if m is None else m, seed, device
         self._ctx = tq_ctx_create(d, bits, self.m, seed, device)
+        if decode_path != "auto":
+            self.set_decode_path(decode_path)
+
+    def set_decode_path(self, path):
+        """'auto', 'simt', 'mma' or 'tc' (TQ_DECODE_*); query workspace sizes afterwards."""
+        code = DECODE_PATHS[path] if isinstance(path, str) else int(path)
+        _check("tq_ctx_set_decode_path", lib().tq_ctx_set_decode_path(self._ctx, code))
+        self.decode_path = path
 
     def close(self):
         if self._ctx:

@@ -239,12 +239,63 @@ extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, i
   return launch_quantize_simt(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
 }
 
+extern "C" int tq_ctx_set_decode_path(tq_ctx* ctx, int path) {
+  if (!ctx) return TQ_EINVAL;
+  switch (path) {
+    case TQ_DECODE_AUTO:
+    case TQ_DECODE_SIMT:
+      break;
+    case TQ_DECODE_MMA:
+      if (ctx->d != 64 && ctx->d != 128 && ctx->d != 256) return TQ_EUNSUPPORTED;
+      break;
+    case TQ_DECODE_TC:
+      if (ctx->d != 128 || (ctx->bits != 2 && ctx->bits != 3)) return TQ_EUNSUPPORTED;
+      break;
+    default:
+      return TQ_EINVAL;
+  }
+  ctx->decode_path = path;
+  return TQ_OK;
+}
+
+namespace {
+
+// Kernel a decode call takes: TQ_DECODE_SIMT / _MMA / _TC, or TQ_EUNSUPPORTED.  The bit-plane
+// kernels share one launch plan (mp).
+int decode_kernel_for(const tq_ctx* ctx, int batch, int q_heads, int kv_heads, int max_tokens, tq::MmaPlan* mp) {
+  tq::MmaPlan pm, pt;
+  const bool mma_ok = tq::plan_decode_mma(ctx, batch, q_heads, kv_heads, max_tokens, &pm);
+  const bool tc_ok = tq::plan_decode_tc(ctx, batch, q_heads, kv_heads, max_tokens, &pt);
+  int kern = TQ_EUNSUPPORTED;
+  switch (ctx->decode_path) {
+    case TQ_DECODE_SIMT:
+      kern = TQ_DECODE_SIMT;
+      break;
+    case TQ_DECODE_MMA:
+      if (mma_ok) kern = TQ_DECODE_MMA;
+      break;
+    case TQ_DECODE_TC:
+      if (tc_ok) kern = TQ_DECODE_TC;
+      break;
+    default:
+      if (tc_ok && (!mma_ok || tq::decode_tc_preferred(ctx, q_heads, kv_heads))) kern = TQ_DECODE_TC;
+      else kern = mma_ok ? TQ_DECODE_MMA : TQ_DECODE_SIMT;
+  }
+  if (kern == TQ_DECODE_MMA) *mp = pm;
+  if (kern == TQ_DECODE_TC) *mp = pt;
+  return kern;
+}
+
+}  // namespace
+
 extern "C" size_t tq_decode_workspace_bytes(const tq_ctx* ctx, int batch, int q_heads, int kv_heads,
                                             int max_tokens) {
   if (!ctx || batch < 1 || q_heads < 1 || kv_heads < 1 || max_tokens < 1) return 0;
+  if (q_heads % kv_heads != 0) return 0;
   tq::MmaPlan mp;
-  if (tq::plan_decode_mma(ctx, batch, q_heads, kv_heads, max_tokens, &mp))
-    return tq::decode_mma_workspace(ctx, mp, batch, q_heads, kv_heads);
+  const int kern = decode_kernel_for(ctx, batch, q_heads, kv_heads, max_tokens, &mp);
+  if (kern == TQ_DECODE_MMA || kern == TQ_DECODE_TC) return tq::decode_mma_workspace(ctx, mp, batch, q_heads, kv_heads);
+  if (kern != TQ_DECODE_SIMT) return 0;
   tq::SplitPlan sp = tq::plan_splits(batch, kv_heads, max_tokens);
   size_t rows = (size_t)batch * q_heads;
   size_t floats = rows * ctx->d * 2 + rows * sp.splits * (2 + ctx->d);
@@ -262,16 +313,17 @@ extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int 
   if (!aligned(q, 16) || !aligned(cache, 256) || !aligned(out, 16) || !aligned(workspace, 256) ||
       !aligned(seq_lens, 4) || (logits_out && !aligned(logits_out, 4)))
     return TQ_EINVAL;
+  tq::MmaPlan mp;
+  const int kern = decode_kernel_for(ctx, batch, q_heads, kv_heads, max_tokens, &mp);
+  if (kern < 0) return kern;
   if (workspace_bytes < tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens)) return TQ_ENOMEM;
   DeviceGuard guard(ctx->device);
-  tq::MmaPlan mp;
-  if (tq::plan_decode_mma(ctx, batch, q_heads, kv_heads, max_tokens, &mp)) {
-    if (tq::decode_tc_supported(ctx, q_heads, kv_heads))
-      return tq::launch_decode_tc(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
-                                  workspace, stream);
+  if (kern == TQ_DECODE_TC)
+    return tq::launch_decode_tc(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
+                                workspace, stream);
+  if (kern == TQ_DECODE_MMA)
     return tq::launch_decode_mma(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
                                  workspace, stream);
-  }
   return launch_decode_simt(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
                             workspace, stream);
 }

@@ -4,6 +4,25 @@
 #include "decode_mma.cuh"
 
 namespace tq {
+
+// Balanced split of all pages of all (batch, kv head) sequences over at most `ctas` CTAs:
+// every CTA takes `chunk` consecutive pages, which may span sequence boundaries.
+bool plan_pages(long ctas, int batch, int kv_heads, int max_tokens, MmaPlan* p) {
+  const long pm = (max_tokens + 127) / 128;
+  const long total = (long)batch * kv_heads * pm;
+  if (total > 0x7fffffffL || total < 1) return false;
+  long grid = total < ctas ? total : ctas;
+  if (grid < 1) grid = 1;
+  long chunk = (total + grid - 1) / grid;
+  grid = (total + chunk - 1) / chunk;
+  p->pages_per_seq = (int)pm;
+  p->total_pages = (int)total;
+  p->chunk = (int)chunk;
+  p->grid = (int)grid;
+  p->slots = (int)((pm - 1) / chunk + 2);
+  return true;
+}
+
 namespace dmma {
 
 // Merges the partial records of one (query head, batch) and rotates back: out = Pi^T o~ / l.
@@ -69,20 +88,7 @@ bool plan_one(const tq_ctx* c, int batch, int kv_heads, int max_tokens, MmaPlan*
   if constexpr (!C::SUPPORTED) {
     return false;
   } else {
-    const long pm = (max_tokens + 127) / 128;
-    const long total = (long)batch * kv_heads * pm;
-    if (total > 0x7fffffffL) return false;
-    long cap = (long)c->num_sms * C::MINB;
-    long grid = total < cap ? total : cap;
-    if (grid < 1) grid = 1;
-    long chunk = (total + grid - 1) / grid;
-    grid = (total + chunk - 1) / chunk;
-    p->pages_per_seq = (int)pm;
-    p->total_pages = (int)total;
-    p->chunk = (int)chunk;
-    p->grid = (int)grid;
-    p->slots = (int)((pm - 1) / chunk + 2);
-    return true;
+    return plan_pages((long)c->num_sms * C::MINB, batch, kv_heads, max_tokens, p);
   }
 }
 
@@ -246,10 +252,6 @@ int tc_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
 
 bool decode_tc_supported(const tq_ctx* c, int q_heads, int kv_heads) {
   if (c->d != 128 || q_heads % kv_heads != 0) return false;
-  // A tcgen05.mma of M = 128, K = 32 costs about the same for every N up to 64, so the
-  // tensor-memory kernel pays off only when a KV head carries many query heads; with up
-  // to 8 the mma.sync kernel is faster on B300.
-  if (q_heads / kv_heads <= 8) return false;
   const int gp = tc_gp(q_heads / kv_heads);
   if (gp == 0) return false;
 #define TQ_S(BB, GG) \
@@ -257,6 +259,14 @@ bool decode_tc_supported(const tq_ctx* c, int q_heads, int kv_heads) {
   TQ_S(2, 4) TQ_S(2, 8) TQ_S(2, 16) TQ_S(3, 4) TQ_S(3, 8) TQ_S(3, 16)
 #undef TQ_S
   return false;
+}
+
+bool plan_decode_tc(const tq_ctx* c, int batch, int q_heads, int kv_heads, int max_tokens, MmaPlan* p) {
+  return decode_tc_supported(c, q_heads, kv_heads) && plan_pages(c->num_sms, batch, kv_heads, max_tokens, p);
+}
+
+bool decode_tc_preferred(const tq_ctx* c, int q_heads, int kv_heads) {
+  return decode_tc_supported(c, q_heads, kv_heads);
 }
 
 int prepare_decode_tc(const tq_ctx* c) {

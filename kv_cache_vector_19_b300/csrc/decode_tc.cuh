@@ -15,11 +15,16 @@
 // the values) and the tensor pipe runs them asynchronously; completion is signalled on
 // mbarriers by tcgen05.commit.
 //
-// Warp roles, 8 warps: warps 0-3 ("token warps", TMEM lane = token) read D_s, form logits,
-// run the lazy online softmax and write B_v; warps 4-7 ("plane warps", same lane quarters)
-// expand the value planes of page p (lane = coordinate) and the key planes of page p+1
-// (lane = token) into TMEM.  Per page: one CTA barrier, after which the elected thread
-// issues the value MMA of page p and the score MMA of page p+1 and refills the page ring.
+// Warp roles, 16 warps, handing work over through mbarriers (no CTA barrier per page):
+//   warps 0-3   token warps (TMEM lane = token): read D_s, form logits, run the lazy online
+//               softmax, write B_v and, when the running maximum moves, rescale D_v
+//   warps 4-7   key-plane warps (lane = token): key XOR planes and the sign plane -> A_s
+//   warps 8-11  value-plane warps (lane = coordinate): value XOR planes -> A_v; epilogue
+//   warp 12     issues the score MMAs, warp 13 the value MMAs (one lane each)
+//   warp 14     keeps the page ring filled with cp.async.bulk
+// Each plane has its own ready / done barrier pair, so the planes of page p+1 are stored
+// while the MMAs of page p still read the other planes.  A tcgen05.mma of M = 128, K = 32
+// costs ~47 cycles for any N up to 64 on B300; the 28 MMAs of a page (b = 3) are the floor.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -39,8 +44,12 @@ namespace dtc {
 using namespace dev;
 using dmma::Params;
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;            // 4 token, 4 key-plane, 4 value-plane, 2 issuers, 2 waiters
 constexpr int kThreads = kWarps * 32;
+constexpr int kWarpS = 12;            // issues the score MMAs
+constexpr int kWarpM = 13;            // issues the value MMAs
+constexpr int kWarpWS = 14;           // waits for the score operands, hands them to kWarpS
+constexpr int kWarpWM = 15;           // waits for the value operands, hands them to kWarpM; page ring
 constexpr int kL2Ahead = 12;
 constexpr float kTau = 3.0f;          // lazy-maximum threshold (natural-log units)
 constexpr float kSB = 2.0f;           // e4m3 range scale of the softmax weights
@@ -56,29 +65,35 @@ struct Cfg {
   static constexpr int NHALF = rnd(3 * GP, 8);         // score columns: [key term | sign term]
   static constexpr int NSC = rnd(2 * NHALF, 16);
   static constexpr int NVC = 2 * GP < 16 ? 16 : 2 * GP;  // value columns: 2 pieces per head
-  // tensor-memory columns
+  // tensor-memory columns: D_s (double-buffered when it fits), D_v, A_s, A_v
+  static constexpr int DS_COLS = rnd(NSC, 32);
+  static constexpr int DV_COLS = rnd(PV * NVC, 32);
+  static constexpr int DSB = 2 * DS_COLS + DV_COLS + (NS + PV) * 32 <= 512 ? 2 : 1;
   static constexpr int TD_S = 0;
-  static constexpr int TD_V = rnd(NSC, 32);
-  static constexpr int TA_S = TD_V + rnd(PV * NVC, 32);
+  static constexpr int TD_V = DSB * DS_COLS;
+  static constexpr int TA_S = TD_V + DV_COLS;
   static constexpr int TA_V = TA_S + NS * 32;
   static constexpr int TCOLS = TA_V + PV * 32;
   static constexpr int TALLOC = TCOLS <= 256 ? 256 : 512;
   // shared memory
   static constexpr int PAGE = PL::bytes;
-  static constexpr int NBUF = (128 * 1024) / PAGE > 8 ? 8 : (128 * 1024) / PAGE;
+  static constexpr int NBUF = (120 * 1024) / PAGE > 8 ? 8 : (120 * 1024) / PAGE;
   static constexpr int BS_BYTES = NSC * NS * 128;
-  static constexpr int BV_BYTES = NVC * 128;
+  static constexpr int BV_BYTES = NVC * 128;                    // per buffer, 2 buffers
   static constexpr int OFF_PAGES = 0;
   static constexpr int OFF_BS = OFF_PAGES + NBUF * PAGE;
   static constexpr int OFF_BV = OFF_BS + BS_BYTES;
-  static constexpr int OFF_Q = OFF_BV + BV_BYTES;               // [GP][2][128] f32
+  static constexpr int OFF_Q = OFF_BV + 2 * BV_BYTES;           // [GP][2][128] f32
   static constexpr int OFF_HEAD = OFF_Q + GP * 2 * 128 * 4;     // [GP][8] f32
   static constexpr int OFF_RED = OFF_HEAD + GP * 8 * 4;         // [4 warps][GP + 1][3] f32
-  static constexpr int OFF_F = OFF_RED + 4 * (GP + 1) * 3 * 4;  // [GP] rescale factors, [GP] n_ref
-  static constexpr int OFF_MBAR = rnd(OFF_F + (GP + 1) * 4, 8); // full[NBUF], s_done, v_done
-  static constexpr int OFF_MISC = OFF_MBAR + (NBUF + 2) * 8;    // tmem base, fail, rescale
+  static constexpr int OFF_F = OFF_RED + 4 * (GP + 1) * 3 * 4;  // n_ref of the segment
+  static constexpr int OFF_MBAR = rnd(OFF_F + 16, 8);
+  // full[NBUF], empty[NBUF], as_ready[NS], s_pl[NS], ds_free[2], av_ready[PV], v_pl[PV],
+  // bv_ready[2], s_fin[2], v_fin[2], teardown[2]
+  static constexpr int NMBAR = 2 * NBUF + 2 * NS + 2 * PV + 10;
+  static constexpr int OFF_MISC = OFF_MBAR + NMBAR * 8;         // tmem base, fail
   static constexpr int SMEM = OFF_MISC + 16;
-  static constexpr bool SUPPORTED = TCOLS <= 512 && SMEM <= 225 * 1024 && NBUF >= 4;
+  static constexpr bool SUPPORTED = TCOLS <= 512 && SMEM <= 225 * 1024 && NBUF >= 4 && NS <= 3 && PV <= 4;
 };
 
 // OR-vote / barrier among the four token warps (named barrier 1).
@@ -93,6 +108,21 @@ __device__ __forceinline__ int t_vote_or(int pred) {
 }
 __device__ __forceinline__ void t_sync() { asm volatile("barrier.cta.sync 1, 128;" ::: "memory"); }
 
+// The two MMA-issuing warps never wait on an mbarrier: on B300 a shared-memory access by a
+// thread with MMAs in flight (an mbarrier wait included) stalls it for hundreds of cycles,
+// while a named barrier does not.  A waiter warp polls the mbarriers (bounded waits) and then
+// meets its issuer at a named barrier that both sync, so the two stay in lock step and every
+// sync has a partner even after a timeout.  Ids: 1 token-warp sync, 2 score pair, 3 value pair.
+constexpr int kNbScore = 2;
+constexpr int kNbValue = 3;
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void pair_sync(int id) {
+  __syncwarp();
+  asm volatile("barrier.cta.sync.aligned %0, 64;" ::"r"(id) : "memory");
+}
+
 // bit position (0..7) of coordinate or token slot x within its plane word
 __host__ __device__ __forceinline__ int kpos_of(int x) { return 2 * (x >> 5) + ((x >> 4) & 1); }
 // coordinate / token slot held by byte e of TMEM column (w * 8 + k) of a plane
@@ -100,12 +130,33 @@ __host__ __device__ __forceinline__ int slot_of_col(int w, int k, int e) {
   return 32 * (k >> 1) + 16 * (k & 1) + 4 * w + e;
 }
 
+// XOR of the code words selected by odd subset `pl`, expanded to 32 e4m3 columns and stored
+// into this warp's lane quarter of a tensor-memory plane.
+template <int NB>
+__device__ __forceinline__ void plane_to_tmem(const uint4 (&w)[NB], int pl, uint32_t taddr) {
+  uint32_t x[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int q = 0; q < NB; ++q)
+    if ((mono_mask16(pl) >> q) & 1) {
+      x[0] ^= w[q].x;
+      x[1] ^= w[q].y;
+      x[2] ^= w[q].z;
+      x[3] ^= w[q].w;
+    }
+  uint32_t r[32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r[8 * c + k] = expand_at(x[c], k);
+  tmem_st32(taddr, r);
+}
+
 template <int BITS, int GP>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
   using C = Cfg<BITS, GP>;
   using PL = typename C::PL;
   constexpr int D = 128, NS = C::NS, PK = C::PK, PV = C::PV, BK = C::BK, BV = C::BV, NBUF = C::NBUF;
-  constexpr int NSC = C::NSC, NVC = C::NVC, NHALF = C::NHALF;
+  constexpr int NSC = C::NSC, NVC = C::NVC, NHALF = C::NHALF, DSB = C::DSB;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint8_t* s_pages = smem + C::OFF_PAGES;
   uint8_t* s_bs = smem + C::OFF_BS;
@@ -114,16 +165,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
   float* s_head = reinterpret_cast<float*>(smem + C::OFF_HEAD);
   float* s_red = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* s_f = reinterpret_cast<float*>(smem + C::OFF_F);
-  uint64_t* s_full = reinterpret_cast<uint64_t*>(smem + C::OFF_MBAR);
-  uint64_t* s_sdone = s_full + NBUF;
-  uint64_t* s_vdone = s_full + NBUF + 1;
+  uint64_t* mb = reinterpret_cast<uint64_t*>(smem + C::OFF_MBAR);
+  uint64_t* s_full = mb;                   // page in slot landed (loader, + tx bytes)
+  uint64_t* s_empty = mb + NBUF;           // page in slot read by every consumer warp (12)
+  uint64_t* as_ready = mb + 2 * NBUF;      // [NS] key plane stored in A_s (4 key-plane warps)
+  uint64_t* s_pl = as_ready + NS;          // [NS] score MMAs reading key plane done (commit)
+  uint64_t* ds_free = s_pl + NS;           // [2] D_s buffer read by the token warps (4)
+  uint64_t* av_ready = ds_free + 2;        // [PV] value plane stored in A_v (4 value-plane warps)
+  uint64_t* v_pl = av_ready + PV;          // [PV] value MMAs reading value plane done (commit)
+  uint64_t* bv_ready = v_pl + PV;          // [2] B_v buffer written, D_v rescaled (4 token warps)
+  // [2] every score MMA of a page done, one barrier per D_s buffer; [2] every value MMA of a
+  // page done, one barrier per page parity.  Waiting on these keeps each barrier at most one
+  // phase ahead of its waiter, so a parity wait never mistakes an older phase for a newer one.
+  uint64_t* s_fin = bv_ready + 2;
+  uint64_t* v_fin = s_fin + 2;
+  uint64_t* td_bar = v_fin + 2;            // [2] teardown drains of the two MMA issuers
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* s_fail = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  volatile int* s_rescale = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool tok = warp < 4;                 // token warps
-  const int row = 32 * (warp & 3) + lane;    // TMEM lane of this thread
+  const int row = 32 * (warp & 3) + lane;    // TMEM lane of this thread (4-warp roles)
   const int G = a.group, PM = a.pages_per_seq;
   const float inv_sqrt_d = rsqrtf((float)D);
   const float qjl_c = 1.2533141373155002512f / (float)D;   // sqrt(pi/2) / m, m = d
@@ -134,9 +195,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
 
   if (warp == 0) tmem_alloc(s_tmem, C::TALLOC);
   if (tid == 0) {
-    for (int i = 0; i < NBUF + 2; ++i) mbar_init(&s_full[i], 1);
+    for (int i = 0; i < NBUF; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 12);
+    }
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&as_ready[i], 4);
+      mbar_init(&s_pl[i], 1);
+    }
+    for (int i = 0; i < PV; ++i) {
+      mbar_init(&av_ready[i], 4);
+      mbar_init(&v_pl[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ds_free[i], 4);
+      mbar_init(&bv_ready[i], 4);
+      mbar_init(&s_fin[i], 1);
+      mbar_init(&v_fin[i], 1);
+      mbar_init(&td_bar[i], 1);
+    }
     *s_fail = 0;
-    *s_rescale = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
@@ -151,19 +229,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
   constexpr uint32_t idesc_s = make_idesc(0, 0, 128, NSC);
   constexpr uint32_t idesc_v = make_idesc(0, 0, 128, NVC);
 
-  uint32_t fill_count = 0;   // pages issued into the ring (all segments)
-  uint32_t waited = 0;       // ring fills this thread has seen complete
-  uint32_t issued = 0;       // ring fills issued (thread 0)
-  uint32_t n_s = 0, n_v = 0; // MMA groups committed on s_done / v_done (all segments)
-  bool failed = false;
+  // every hand-off barrier completes once per page; pages are counted over all segments
+  uint32_t pg_base = 0;      // pages (== ring fills) of the previous segments
+  uint32_t issued = 0;       // ring fills issued (loader lane)
 
   auto fail_now = [&]() {
     if (lane == 0) atomicOr(a.status, kFlagTimeout);
     *s_fail = 1;
   };
+  // bounded wait for the k-th completion (0-based) of a barrier that completes once per use
+  // Once a wait timed out every later wait returns at once: all roles still run their loops
+  // to the end, so the named-barrier counts stay balanced and the kernel finishes.
+  auto wait_k = [&](uint64_t* bar, uint32_t k) {
+    if (*s_fail) return;
+    if (!mbar_wait(bar, k & 1)) fail_now();
+  };
 
   int gp = range_lo;
-  while (gp < range_hi && !failed) {
+  bool s_fail_seen = false;   // read after a CTA barrier, so uniform
+  while (gp < range_hi && !s_fail_seen) {
     const int seq = gp / PM;
     const int seg_lo = gp - seq * PM;
     const int seg_hi = min(range_hi, (seq + 1) * PM) - seq * PM;
@@ -179,22 +263,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
     const int slot = blockIdx.x - (seq * PM) / a.chunk;
     float* rec = a.part + ((size_t)seq * a.slots + slot) * G * (2 + D);
     const uint8_t* seq_base = a.cache + (size_t)seq * PM * PL::bytes;
+    auto ring_slot = [&](int p) { return (pg_base + p) % NBUF; };
+    auto ring_use = [&](int p) { return (pg_base + p) / NBUF; };
+    auto pg_ptr = [&](int p) { return s_pages + ring_slot(p) * C::PAGE; };
 
-    __syncthreads();   // previous segment fully done with shared memory
-    const uint32_t fill_base = fill_count;
-    if (tid == 0) {
+    __syncthreads();   // previous segment fully done
+    if (warp == kWarpWM && lane == 0) {
       const int first = min(n_pages, NBUF);
-      issued = fill_base + first;
       for (int i = 0; i < first; ++i) {
-        const uint32_t si = (fill_base + i) % NBUF;
+        const uint32_t si = ring_slot(i);
         fence_proxy_async();
         mbar_expect_tx(&s_full[si], PL::bytes);
         bulk_g2s(s_pages + si * C::PAGE, seq_base + (size_t)(p_lo + i) * PL::bytes, PL::bytes, &s_full[si]);
       }
+      issued = pg_base + first;
       for (int i = NBUF; i < min(n_pages, NBUF + kL2Ahead); ++i)
         prefetch_l2(seq_base + (size_t)(p_lo + i) * PL::bytes, PL::bytes);
     }
-    fill_count = fill_base + n_pages;
 
     // ---- query operand of this KV head ----
     for (int e = tid; e < GP * 2 * D; e += kThreads) {
@@ -294,156 +379,194 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
     fence_proxy_async();   // B_s is read by the tensor cores
     __syncthreads();
 
-    // ---- running state (token warps; identical in every token thread) ----
-    float m_run[GP], l_part[GP], c_part[GP], g_part[GP];
-#pragma unroll
-    for (int h = 0; h < GP; ++h) {
-      m_run[h] = -INFINITY;
-      l_part[h] = c_part[h] = g_part[h] = 0.f;
+    // token-warp form of the per-head constants: 1/s_k, 1/s_q, C_k, C_q, asum_k * sum q~, sum q_s
+    for (int hh = tid; hh < GP; hh += kThreads) {
+      float* hp = s_head + hh * 8;
+      hp[0] = 1.f / hp[0];
+      hp[1] = 1.f / hp[1];
+      hp[4] = a.asum_k * hp[4];
     }
-    float n_ref = 0.f;
+    __syncthreads();
 
-    auto wait_full = [&](int p) {
-      const uint32_t fi = fill_base + p;
-      if (mbar_wait(&s_full[fi % NBUF], (fi / NBUF) & 1)) {
-        if (fi + 1 > waited) waited = fi + 1;
-      } else {
-        fail_now();
-      }
-    };
-    // plane warps: key planes and sign plane of token `row` of page p -> A_s
-    auto load_keys = [&](int p) {
-      const uint8_t* pg = s_pages + ((fill_base + p) % NBUF) * C::PAGE;
-      uint4 wk[BK];
-#pragma unroll
-      for (int q = 0; q < BK; ++q)
-        wk[q] = *reinterpret_cast<const uint4*>(pg + PL::off_kcodes + ((size_t)q * 128 + row) * 16);
-      const uint4 wsg = *reinterpret_cast<const uint4*>(pg + PL::off_signs + (size_t)row * 16);
-#pragma unroll
-      for (int pl = 0; pl < NS; ++pl) {
-        uint32_t x[4];
-        if (pl < PK) {
-          x[0] = x[1] = x[2] = x[3] = 0u;
-#pragma unroll
-          for (int q = 0; q < BK; ++q)
-            if ((mono_mask16(pl) >> q) & 1) {
-              x[0] ^= wk[q].x;
-              x[1] ^= wk[q].y;
-              x[2] ^= wk[q].z;
-              x[3] ^= wk[q].w;
-            }
-        } else {
-          x[0] = wsg.x;
-          x[1] = wsg.y;
-          x[2] = wsg.z;
-          x[3] = wsg.w;
-        }
-        uint32_t r[32];
-#pragma unroll
-        for (int w = 0; w < 4; ++w)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) r[8 * w + k] = expand_at(x[w], k);
-        tmem_st32(tl + C::TA_S + 32 * pl, r);
-      }
-    };
-    // plane warps: value planes of coordinate `row` of page p -> A_v
-    auto load_values = [&](int p) {
-      const uint8_t* pg = s_pages + ((fill_base + p) % NBUF) * C::PAGE;
-      uint4 wv[BV];
-#pragma unroll
-      for (int q = 0; q < BV; ++q)
-        wv[q] = *reinterpret_cast<const uint4*>(pg + PL::off_vcodes + ((size_t)q * D + row) * 16);
-#pragma unroll
-      for (int pl = 0; pl < PV; ++pl) {
-        uint32_t x[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int q = 0; q < BV; ++q)
-          if ((mono_mask16(pl) >> q) & 1) {
-            x[0] ^= wv[q].x;
-            x[1] ^= wv[q].y;
-            x[2] ^= wv[q].z;
-            x[3] ^= wv[q].w;
-          }
-        uint32_t r[32];
-#pragma unroll
-        for (int w = 0; w < 4; ++w)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) r[8 * w + k] = expand_at(x[w], k);
-        tmem_st32(tl + C::TA_V + 32 * pl, r);
-      }
-    };
-    auto issue_score = [&]() {   // elected thread
-      tc_fence_after();
-#pragma unroll 1
-      for (int ks = 0; ks < NS * 4; ++ks) {
-        const uint64_t bd = smem_desc(smem_u32(s_bs) + ks * 256, 128, NS * 1024);
-        mma_f8_ts(tmem + C::TD_S, tmem + C::TA_S + 8 * ks, bd, idesc_s, ks > 0);
-      }
-      tc_commit(s_sdone);
-    };
-    auto issue_values = [&](bool first_page) {   // elected thread
-      tc_fence_after();
-#pragma unroll 1
-      for (int pl = 0; pl < PV; ++pl)
-#pragma unroll 1
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = smem_desc(smem_u32(s_bv) + ks * 256, 128, 1024);
-          mma_f8_ts(tmem + C::TD_V + pl * NVC, tmem + C::TA_V + 32 * pl + 8 * ks, bd, idesc_v,
-                    !(first_page && ks == 0));
-        }
-      tc_commit(s_vdone);
-    };
 
     if (n_pages > 0) {
-      // prologue: plane warps put the keys of page 0 into A_s
-      if (!tok) {
-        wait_full(0);
-        load_keys(0);
-        tc_wait_st();
-      }
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) issue_score();
-      ++n_s;
-
-      for (int p = 0; p < n_pages; ++p) {
-        const uint8_t* pg = s_pages + ((fill_base + p) % NBUF) * C::PAGE;
-        if (tok) {
-          // ---------- token warps: logits, lazy softmax, softmax-weight operand ----------
-          wait_full(p);
-          if (!mbar_wait(s_sdone, (n_s - 1) & 1)) fail_now();
+      if (warp == kWarpWS) {
+        // ============ score waiter: operands of the next plane ready -> meet the score issuer ============
+        for (int p = 0; p < n_pages; ++p) {
+          const uint32_t g = pg_base + p, db = DSB == 2 ? (g & 1) : 0;
+#pragma unroll 1
+          for (int pl = 0; pl < NS; ++pl) {
+            wait_k(&as_ready[pl], g);
+            if (pl == 0 && g >= (uint32_t)DSB) wait_k(&ds_free[db], g / DSB - 1);
+            pair_sync(kNbScore);
+          }
+        }
+      } else if (warp == kWarpS) {
+        // ============ score MMAs: D_s[token][column] = sum over planes of A_s(plane) x B_s ============
+        const uint32_t bs = smem_u32(s_bs);
+        for (int p = 0; p < n_pages; ++p) {
+          const uint32_t g = pg_base + p, db = DSB == 2 ? (g & 1) : 0;
+#pragma unroll 1
+          for (int pl = 0; pl < NS; ++pl) {
+            pair_sync(kNbScore);
+            if (lane == 0) {
+              tc_fence_after();
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                mma_f8_ts(tmem + C::TD_S + db * C::DS_COLS, tmem + C::TA_S + 32 * pl + 8 * ks,
+                          smem_desc(bs + (4 * pl + ks) * 256, 128, NS * 1024), idesc_s, pl > 0 || ks > 0);
+              tc_commit(&s_pl[pl]);
+            }
+          }
+          if (lane == 0) tc_commit(&s_fin[db]);
+        }
+      } else if (warp == kWarpWM) {
+        // ============ value waiter: operands ready -> meet the value issuer; page ring refills ============
+        for (int p = 0; p < n_pages; ++p) {
+          const uint32_t g = pg_base + p;
+          wait_k(&bv_ready[g & 1], g >> 1);
+          pair_sync(kNbValue);
+#pragma unroll 1
+          for (int pl = 0; pl < PV; ++pl) {
+            wait_k(&av_ready[pl], g);
+            pair_sync(kNbValue);
+          }
+          // every consumer has read page p by now: its slot takes page p + NBUF
+          if (lane == 0 && p + NBUF < n_pages) {
+            wait_k(&s_empty[ring_slot(p)], ring_use(p));
+            const int nxt = p + NBUF;
+            const uint32_t si = ring_slot(nxt);
+            fence_proxy_async();
+            mbar_expect_tx(&s_full[si], PL::bytes);
+            bulk_g2s(s_pages + si * C::PAGE, seq_base + (size_t)(p_lo + nxt) * PL::bytes, PL::bytes, &s_full[si]);
+            issued = pg_base + nxt + 1;
+            if (nxt + kL2Ahead < n_pages)
+              prefetch_l2(seq_base + (size_t)(p_lo + nxt + kL2Ahead) * PL::bytes, PL::bytes);
+          }
+          __syncwarp();
+        }
+      } else if (warp == kWarpM) {
+        // ============ value MMAs: D_v(plane)[coordinate][column] += A_v(plane) x B_v ============
+        for (int p = 0; p < n_pages; ++p) {
+          const uint32_t g = pg_base + p;
+          pair_sync(kNbValue);   // B_v(p) written, D_v rescaled
+          const uint32_t bva = smem_u32(s_bv + (g & 1) * C::BV_BYTES);
+#pragma unroll 1
+          for (int pl = 0; pl < PV; ++pl) {
+            pair_sync(kNbValue);
+            if (lane == 0) {
+              tc_fence_after();
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                mma_f8_ts(tmem + C::TD_V + pl * NVC, tmem + C::TA_V + 32 * pl + 8 * ks,
+                          smem_desc(bva + ks * 256, 128, 1024), idesc_v, !(p == 0 && ks == 0));
+              tc_commit(&v_pl[pl]);
+            }
+          }
+          if (lane == 0) tc_commit(&v_fin[g & 1]);
+        }
+      } else if (warp >= 4 && warp < 8) {
+        // ============ key-plane warps (lane = token): XOR planes and the sign plane -> A_s ============
+        for (int p = 0; p < n_pages; ++p) {
+          const uint32_t g = pg_base + p;
+          wait_k(&s_full[ring_slot(p)], ring_use(p));
+          const uint8_t* pgp = pg_ptr(p);
+          uint4 wk[BK + 1];
+#pragma unroll
+          for (int q = 0; q < BK; ++q)
+            wk[q] = *reinterpret_cast<const uint4*>(pgp + PL::off_kcodes + ((size_t)q * 128 + row) * 16);
+          wk[BK] = *reinterpret_cast<const uint4*>(pgp + PL::off_signs + (size_t)row * 16);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
+#pragma unroll
+          for (int pl = 0; pl < NS; ++pl) {
+            if (g > 0) wait_k(&s_pl[pl], g - 1);   // the previous page's MMAs on this plane are done
+            tc_fence_after();
+            if (pl < PK) {
+              plane_to_tmem<BK>(reinterpret_cast<const uint4(&)[BK]>(wk), pl, tl + C::TA_S + 32 * pl);
+            } else {
+              const uint4 ws1[1] = {wk[BK]};
+              plane_to_tmem<1>(ws1, 0, tl + C::TA_S + 32 * pl);
+            }
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&as_ready[pl]);
+          }
+        }
+      } else if (warp >= 8 && warp < 12) {
+        // ============ value-plane warps (lane = coordinate): XOR planes -> A_v ============
+        for (int p = 0; p < n_pages; ++p) {
+          const uint32_t g = pg_base + p;
+          wait_k(&s_full[ring_slot(p)], ring_use(p));
+          const uint8_t* pgp = pg_ptr(p);
+          uint4 wv[BV];
+#pragma unroll
+          for (int q = 0; q < BV; ++q)
+            wv[q] = *reinterpret_cast<const uint4*>(pgp + PL::off_vcodes + ((size_t)q * D + row) * 16);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
+#pragma unroll
+          for (int pl = 0; pl < PV; ++pl) {
+            if (g > 0) wait_k(&v_pl[pl], g - 1);
+            tc_fence_after();
+            plane_to_tmem<BV>(wv, pl, tl + C::TA_V + 32 * pl);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&av_ready[pl]);
+          }
+        }
+      } else if (warp < 4) {
+        // ============ token warps (lane = token): logits, lazy softmax, weight operand ============
+        float m_run[GP], l_part[GP], c_part[GP], g_part[GP];
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+          m_run[h] = -INFINITY;
+          l_part[h] = c_part[h] = g_part[h] = 0.f;
+        }
+        float n_ref = 0.f;
+        for (int p = 0; p < n_pages; ++p) {
+          const uint32_t g = pg_base + p, db = DSB == 2 ? (g & 1) : 0;
+          const uint8_t* pgp = pg_ptr(p);
+          wait_k(&s_full[ring_slot(p)], ring_use(p));
+          wait_k(&s_fin[db], DSB == 2 ? g >> 1 : g);   // every score MMA of page p is done
           tc_fence_after();
           float ds[NSC];
 #pragma unroll
           for (int c0 = 0; c0 < NSC; c0 += 16) {
             uint32_t r[16];
-            tmem_ld16(tl + C::TD_S + c0, r);
+            tmem_ld16(tl + C::TD_S + db * C::DS_COLS + c0, r);
             tc_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) ds[c0 + i] = __uint_as_float(r[i]);
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ds_free[db]);
           const int nvalid = min(128, seq_len - (p_lo + p) * 128);
           const bool valid = row < nvalid;
-          const float nk = valid ? reinterpret_cast<const float*>(pg + PL::off_nk)[row] : 0.f;
-          const float gmv = valid ? reinterpret_cast<const float*>(pg + PL::off_gamma)[row] : 0.f;
-          const float nvt = valid ? reinterpret_cast<const float*>(pg + PL::off_nv)[row] : 0.f;
+          const float nk = valid ? reinterpret_cast<const float*>(pgp + PL::off_nk)[row] : 0.f;
+          const float gmv = valid ? reinterpret_cast<const float*>(pgp + PL::off_gamma)[row] : 0.f;
+          const float nvt = valid ? reinterpret_cast<const float*>(pgp + PL::off_nv)[row] : 0.f;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
           float lg[GP];
           int ovf = nvt > n_ref;
 #pragma unroll
           for (int h = 0; h < GP; ++h) {
-            const float* hp = s_head + h * 8;
+            const float* hp = s_head + h * 8;   // 1/s_k, 1/s_q, C_k, C_q, asum_k * sum q~, sum q_s
             const float mse = ds[3 * h] + 0.0625f * ds[3 * h + 1] + 0.00390625f * ds[3 * h + 2];
             const float qjl = ds[NHALF + 3 * h] + 0.0625f * ds[NHALF + 3 * h + 1] + 0.00390625f * ds[NHALF + 3 * h + 2];
-            const float dk = (mse - hp[2]) / hp[0] - a.asum_k * hp[4];
-            const float dq = (qjl - hp[3]) / hp[1] - hp[5];
-            const float l = (nk * dk + gmv * qjl_c * dq) * inv_sqrt_d;
+            const float dk = fmaf(mse - hp[2], hp[0], -hp[4]);
+            const float dq = fmaf(qjl - hp[3], hp[1], -hp[5]);
+            const float l = fmaf(nk, dk, gmv * qjl_c * dq) * inv_sqrt_d;
             lg[h] = (valid && h < G) ? l : -INFINITY;
             if (a.logits && valid && h < G)
               a.logits[((size_t)b * a.q_heads + (size_t)kvh * G + h) * a.max_tokens + (size_t)(p_lo + p) * 128 + row] = l;
             if (lg[h] > m_run[h] + kTau) ovf = 1;
           }
           if (t_vote_or(ovf)) {
-            // exact page maxima over the 128 token threads, new references, rescale factors
 #pragma unroll
             for (int h = 0; h <= GP; ++h) {
               float mx = h < GP ? lg[h] : nvt;
@@ -455,28 +578,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
             float nvmax = 0.f;
             for (int w2 = 0; w2 < 4; ++w2) nvmax = fmaxf(nvmax, s_red[w2 * (GP + 1) + GP]);
             const float n_new = nvmax > n_ref ? 1.25f * nvmax : n_ref;
+            float fh[GP];
 #pragma unroll
             for (int h = 0; h < GP; ++h) {
               float mx = -INFINITY;
               for (int w2 = 0; w2 < 4; ++w2) mx = fmaxf(mx, s_red[w2 * (GP + 1) + h]);
               const float m_new = fmaxf(m_run[h], mx);
               const float alpha = (m_run[h] == -INFINITY) ? 0.f : __expf(m_run[h] - m_new);
-              const float f = (n_ref > 0.f) ? alpha * (n_ref / n_new) : 0.f;
+              fh[h] = (n_ref > 0.f) ? alpha * (n_ref / n_new) : 0.f;
               l_part[h] *= alpha;
-              c_part[h] *= f;
-              g_part[h] *= f;
-              if (tid == 0) s_f[h] = f;
+              c_part[h] *= fh[h];
+              g_part[h] *= fh[h];
               m_run[h] = m_new;
             }
             n_ref = n_new;
-            if (tid == 0) *s_rescale = 1;
             t_sync();   // s_red reads done
-          } else if (tid == 0) {
-            *s_rescale = 0;
+            if (p > 0) {
+              // D_v holds exactly the pages before p once the value MMAs of page p-1 are done;
+              // this warp rescales its lane quarter (32 coordinates) of every plane accumulator
+              wait_k(&v_fin[(g - 1) & 1], (g - 1) >> 1);
+              tc_fence_after();
+#pragma unroll 1
+              for (int c0 = 0; c0 < PV * NVC; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(tl + C::TD_V + c0, r);
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const int h = ((c0 + i) % NVC) >> 1;
+                  float fv = 0.f;
+#pragma unroll
+                  for (int hh = 0; hh < GP; ++hh) fv = hh == h ? fh[hh] : fv;
+                  r[i] = __float_as_uint(__uint_as_float(r[i]) * fv);
+                }
+                tmem_st16(tl + C::TD_V + c0, r);
+              }
+              tc_wait_st();
+            }
           }
           // softmax weights -> two e4m3 pieces per head; the byte for row n = 2h + piece
-          const float inv_n = n_ref > 0.f ? 1.f / n_ref : 0.f;
-          const float xs = nvt * inv_n * v_igamma * kSB;
+          const float xs = nvt * (n_ref > 0.f ? 1.f / n_ref : 0.f) * v_igamma * kSB;
           uint32_t wb[NVC / 4];
 #pragma unroll
           for (int i = 0; i < NVC / 4; ++i) wb[i] = 0u;
@@ -494,12 +635,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
             wb[(2 * h) >> 2] |= hi << (8 * ((2 * h) & 3));
             wb[(2 * h + 1) >> 2] |= lo << (8 * ((2 * h + 1) & 3));
           }
-          // 4 x 4 byte transposes across the 4 lanes holding tokens 4i .. 4i+3: lane e of the
-          // group ends up with row 4 r + e, bytes = those 4 tokens
+          // B_v buffer of page p: its previous user, the value MMA of page p-2, must be done
+          if (p >= 2) wait_k(&v_fin[g & 1], (g >> 1) - 1);
+          uint8_t* bvb = s_bv + (g & 1) * C::BV_BYTES;
           const int e = lane & 3, base = lane & ~3;
           const int k0 = 32 * ((row >> 2) & 3) + 4 * (row >> 4);   // K byte of token 4i
-          // B_v of the previous page is read by its value MMA: wait for it
-          if (p > 0 && !mbar_wait(s_vdone, (n_v - 1) & 1)) fail_now();
 #pragma unroll
           for (int r4 = 0; r4 < NVC / 4; ++r4) {
             const uint32_t w0 = __shfl_sync(0xffffffffu, wb[r4], base + 0);
@@ -508,100 +648,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
             const uint32_t w3 = __shfl_sync(0xffffffffu, wb[r4], base + 3);
             const uint32_t sel = (uint32_t)e | ((uint32_t)(e + 4) << 4);
             const uint32_t t01 = __byte_perm(w0, w1, sel), t23 = __byte_perm(w2, w3, sel);
-            const uint32_t outw = __byte_perm(t01, t23, 0x5410);
-            *reinterpret_cast<uint32_t*>(s_bv + canon_off(4 * r4 + e, k0, 128)) = outw;
+            *reinterpret_cast<uint32_t*>(bvb + canon_off(4 * r4 + e, k0, 128)) = __byte_perm(t01, t23, 0x5410);
           }
           fence_proxy_async();
-        } else {
-          // ---------- plane warps: values of page p, keys of page p+1 ----------
-          if (p > 0) {
-            if (!mbar_wait(s_vdone, (n_v - 1) & 1)) fail_now();   // A_v free
-            tc_fence_after();
-          }
-          load_values(p);
-          if (p + 1 < n_pages) {
-            wait_full(p + 1);
-            if (!mbar_wait(s_sdone, (n_s - 1) & 1)) fail_now();   // A_s free
-            tc_fence_after();
-            load_keys(p + 1);
-          }
-          tc_wait_st();
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (*s_fail) {
-          failed = true;
-          break;
-        }
-        if (*s_rescale && p > 0) {
-          // D_v holds pages < p (their MMAs are complete): scale it by the new references
-          if (!tok) {
-#pragma unroll 1
-            for (int c0 = 0; c0 < PV * NVC; c0 += 16) {
-              uint32_t r[16];
-              tmem_ld16(tl + C::TD_V + c0, r);
-              tc_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int h = ((c0 + i) % NVC) >> 1;
-                r[i] = __float_as_uint(h < GP ? __uint_as_float(r[i]) * s_f[h] : 0.f);
-              }
-              tmem_st16(tl + C::TD_V + c0, r);
-            }
-            tc_wait_st();
-          }
           tc_fence_before();
-          __syncthreads();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bv_ready[g & 1]);
         }
-        if (tid == 0) {
-          issue_values(p == 0);
-          if (p + 1 < n_pages) issue_score();
-          // ring slot of page p is free: refill
-          const int nxt = p + NBUF;
-          if (nxt < n_pages) {
-            issued = fill_base + nxt + 1;
-            const uint32_t si = (fill_base + nxt) % NBUF;
-            fence_proxy_async();
-            mbar_expect_tx(&s_full[si], PL::bytes);
-            bulk_g2s(s_pages + si * C::PAGE, seq_base + (size_t)(p_lo + nxt) * PL::bytes, PL::bytes, &s_full[si]);
+        // per-head sums of this segment
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+          float v3[3] = {l_part[h], c_part[h], g_part[h]};
+#pragma unroll
+          for (int c = 0; c < 3; ++c) {
+            float v = v3[c];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) s_red[(warp * (GP + 1) + h) * 3 + c] = v;
           }
-          if (nxt + kL2Ahead < n_pages) prefetch_l2(seq_base + (size_t)(p_lo + nxt + kL2Ahead) * PL::bytes, PL::bytes);
         }
-        ++n_v;
-        if (p + 1 < n_pages) ++n_s;
-      }
-    }
-    if (failed) break;
-
-    // ---------- segment epilogue ----------
-    if (tid == 0) s_f[GP] = n_ref;   // the plane warps need the value-norm reference
-    if (tok) {
-#pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        float v3[3] = {l_part[h], c_part[h], g_part[h]};
-#pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          float v = v3[c];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == 0) s_red[(warp * (GP + 1) + h) * 3 + c] = v;
+        if (tid == 0) s_f[0] = n_ref;
+        // partial record head part (m, l)
+        t_sync();
+        if (tid < GP && tid < G) {
+          float l_tot = 0.f;
+          for (int w2 = 0; w2 < 4; ++w2) l_tot += s_red[(w2 * (GP + 1) + tid) * 3];
+          float* rh = rec + (size_t)tid * (2 + D);
+          rh[0] = m_run[tid];
+          rh[1] = l_tot;
         }
       }
     }
-    __syncthreads();
-    if (tok && tid < GP && tid < G) {
-      float l_tot = 0.f;
-      for (int w2 = 0; w2 < 4; ++w2) l_tot += s_red[(w2 * (GP + 1) + tid) * 3];
+    if (n_pages == 0 && warp == 0 && tid < GP && tid < G) {
       float* rh = rec + (size_t)tid * (2 + D);
-      rh[0] = m_run[tid];
-      rh[1] = l_tot;
+      rh[0] = -INFINITY;
+      rh[1] = 0.f;
     }
-    if (!tok) {
+    __syncthreads();   // token sums in s_red
+    if (warp >= 8 && warp < 12) {
+      // ---------- epilogue: o~ = (n_ref / kSB) [ 2 sum_M alpha_M (D_M - C) - sum alpha G ] ----------
       float ov[GP];
 #pragma unroll
       for (int h = 0; h < GP; ++h) ov[h] = 0.f;
       if (n_pages > 0) {
-        if (!mbar_wait(s_vdone, (n_v - 1) & 1)) fail_now();
+        {
+          const uint32_t last = pg_base + n_pages - 1;   // the last value MMA is done
+          wait_k(&v_fin[last & 1], last >> 1);
+        }
         tc_fence_after();
 #pragma unroll 1
         for (int pl = 0; pl < PV; ++pl) {
@@ -619,29 +712,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           }
         }
       }
-      const float nref = s_f[GP];
+      const float nref = n_pages > 0 ? s_f[0] : 0.f;
       const float scale = nref > 0.f ? nref / kSB : 0.f;
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
         if (h >= G) continue;
         float c_tot = 0.f, g_tot = 0.f;
-        for (int w2 = 0; w2 < 4; ++w2) {
-          c_tot += s_red[(w2 * (GP + 1) + h) * 3 + 1];
-          g_tot += s_red[(w2 * (GP + 1) + h) * 3 + 2];
-        }
-        float asum = 0.f;
-        for (int pl = 0; pl < PV; ++pl) asum += a.alpha_v[pl];
-        // o~_j = (n_ref / kSB) [ 2 sum_M alpha_M (D_M - C) - sum alpha G ]
-        const float o = scale * (2.f * (ov[h] - asum * c_tot) - a.asum_v * g_tot);
+        if (n_pages > 0)
+          for (int w2 = 0; w2 < 4; ++w2) {
+            c_tot += s_red[(w2 * (GP + 1) + h) * 3 + 1];
+            g_tot += s_red[(w2 * (GP + 1) + h) * 3 + 2];
+          }
+        const float o = scale * (2.f * (ov[h] - a.asum_v * c_tot) - a.asum_v * g_tot);
         rec[(size_t)h * (2 + D) + 2 + row] = n_pages > 0 ? o : 0.f;
       }
     }
+    pg_base += n_pages;
+    tc_fence_before();
+    __syncthreads();
+    s_fail_seen = *s_fail != 0;
   }
-  // teardown: outstanding copies and MMAs complete (bounded), then free tensor memory
-  if (failed && tid == 0) {
-    for (uint32_t i = waited; i < issued; ++i) mbar_wait(&s_full[i % NBUF], (i / NBUF) & 1);
-    if (n_s > 0) mbar_wait(s_sdone, (n_s - 1) & 1);
-    if (n_v > 0) mbar_wait(s_vdone, (n_v - 1) & 1);
+  // teardown after a timeout: the last fill of each ring slot and every MMA the two issuers
+  // started complete (bounded waits) before the shared and tensor memory are released
+  if (s_fail_seen && lane == 0) {
+    if (warp == kWarpWM)
+      for (uint32_t i = issued > (uint32_t)NBUF ? issued - NBUF : 0u; i < issued; ++i)
+        mbar_wait(&s_full[i % NBUF], (i / NBUF) & 1);
+    if (warp == kWarpS || warp == kWarpM) {
+      uint64_t* t = &td_bar[warp == kWarpS ? 0 : 1];
+      tc_commit(t);
+      mbar_wait(t, 0);
+    }
   }
   tc_fence_before();
   __syncthreads();

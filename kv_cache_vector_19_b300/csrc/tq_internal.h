@@ -60,6 +60,7 @@ struct tq_ctx {
   float* d_alpha_v = nullptr;   // [2^(bits-1)]
   float asum_k = 0.f, asum_v = 0.f;
   int num_sms = 148;
+  int decode_path = 0;   // TQ_DECODE_*
   // head_dim 128: bf16 B operands of the tensor-core quantizer, no-swizzle K-major layout:
   // Pi hi, Pi lo, S' hi, S' lo (each 128 x 128, 32 KB)
   uint8_t* d_qblob = nullptr;
@@ -80,7 +81,9 @@ int launch_quantize_simt(const tq_ctx* ctx, const void* k, const void* v, int ba
                          void* stream);
 namespace tq {
 int prepare_decode_mma(const tq_ctx* c);
+bool plan_pages(long ctas, int batch, int kv_heads, int max_tokens, MmaPlan* p);
 bool plan_decode_mma(const tq_ctx* c, int batch, int q_heads, int kv_heads, int max_tokens, MmaPlan* p);
+bool plan_decode_tc(const tq_ctx* c, int batch, int q_heads, int kv_heads, int max_tokens, MmaPlan* p);
 int launch_decode_mma(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                       const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
                       void* workspace, void* stream);
@@ -88,6 +91,8 @@ size_t decode_mma_workspace(const tq_ctx* c, const MmaPlan& pl, int batch, int q
 // tcgen05 decode (head_dim 128, b in {2, 3}, up to 16 query heads per KV head); same plan,
 // workspace and partial records as the mma.sync kernel.
 bool decode_tc_supported(const tq_ctx* c, int q_heads, int kv_heads);
+// whether TQ_DECODE_AUTO takes the tcgen05 kernel over the mma.sync one (by measurement)
+bool decode_tc_preferred(const tq_ctx* c, int q_heads, int kv_heads);
 int prepare_decode_tc(const tq_ctx* c);
 int launch_decode_tc(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                      const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,

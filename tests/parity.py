@@ -29,10 +29,10 @@ OUT_ON_PAGES_REL_L2 = 5e-3
 class Run:
     """A context plus device buffers for one workload shape."""
 
-    def __init__(self, d, b, batch, kv_heads, q_heads, max_tokens, seed=0):
+    def __init__(self, d, b, batch, kv_heads, q_heads, max_tokens, seed=0, decode_path="auto"):
         self.d, self.b, self.m = d, b, d
         self.batch, self.kv_heads, self.q_heads, self.max_tokens = batch, kv_heads, q_heads, max_tokens
-        self.ctx = tq.Context(d, b, seed=seed)
+        self.ctx = tq.Context(d, b, seed=seed, decode_path=decode_path)
         self.cache = self.ctx.alloc_cache(batch, kv_heads, max_tokens)
         self.ws = self.ctx.alloc_workspace(batch, q_heads, kv_heads, max_tokens)
         self.n_pages = (max_tokens + 127) // 128

@@ -64,6 +64,7 @@ def test_host_argument_checks_need_no_gpu():
     assert L.tq_cache_bytes(None, 1, 1, 1) == 0
     assert L.tq_decode_workspace_bytes(None, 1, 1, 1, 1) == 0
     assert L.tq_get_device_status(None, None) == tq.TQ_EINVAL
+    assert L.tq_ctx_set_decode_path(None, tq.TQ_DECODE_TC) == tq.TQ_EINVAL
     c = (ctypes.c_double * 4)()
     assert L.tq_make_codebook(2, 4, c, c) == tq.TQ_EINVAL
     assert L.tq_make_codebook(128, 65, c, c) == tq.TQ_EINVAL

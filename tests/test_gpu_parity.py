@@ -54,12 +54,10 @@ def test_quantize_small_all_formats(d, b):
             assert P.repack_matches(run, cache, bb, h, page, pg)
 
 
-@pytest.mark.parametrize("d,b,G", [(64, 2, 1), (128, 3, 4), (128, 4, 8), (256, 5, 16), (256, 3, 2),
-                                   (64, 5, 16), (128, 2, 3)])
-def test_decode_small(d, b, G):
+def _check_decode(d, b, G, path="auto"):
     B, H, maxT = 2, 2, 700
     N = 650
-    run = P.Run(d, b, B, H, G * H, maxT)
+    run = P.Run(d, b, B, H, G * H, maxT, decode_path=path)
     k, v = _inputs(B, H, N, d, seed=100 + d + b, scale=1.5)
     run.quantize(k, v, [0, 0])
     q = torch.randn(B, G * H, d, generator=torch.Generator().manual_seed(7))
@@ -80,6 +78,63 @@ def test_decode_small(d, b, G):
                 assert P.rel_l2(out[bb, hq], o_pages) < P.OUT_ON_PAGES_REL_L2
                 o_e2e, _ = P.oracle_end_to_end(run, qrow, res["oracle_k"], res["oracle_v"])
                 assert P.rel_l2(out[bb, hq], o_e2e) < P.OUT_REL_L2
+
+
+@pytest.mark.parametrize("d,b,G", [(64, 2, 1), (128, 3, 4), (128, 4, 8), (256, 5, 16), (256, 3, 2),
+                                   (64, 5, 16), (128, 2, 3)])
+def test_decode_small(d, b, G):
+    _check_decode(d, b, G)
+
+
+# every decode kernel on its own, whatever the automatic choice would be
+@pytest.mark.parametrize("path,d,b,G", [
+    ("simt", 64, 2, 1), ("simt", 128, 3, 4), ("simt", 256, 5, 16),
+    ("mma", 64, 2, 1), ("mma", 128, 3, 4), ("mma", 128, 4, 8), ("mma", 128, 3, 16), ("mma", 128, 2, 3),
+    ("mma", 128, 5, 2), ("mma", 256, 4, 1),
+    ("tc", 128, 3, 4), ("tc", 128, 3, 8), ("tc", 128, 3, 16), ("tc", 128, 2, 3), ("tc", 128, 2, 16),
+    ("tc", 128, 3, 1)])
+def test_decode_small_each_kernel(path, d, b, G):
+    _check_decode(d, b, G, path)
+
+
+def test_decode_path_selection():
+    ctx = tq.Context(64, 4)
+    with pytest.raises(tq.TQError) as e:
+        ctx.set_decode_path("tc")          # head dim 64 has no tcgen05 kernel
+    assert e.value.status == tq.TQ_EUNSUPPORTED
+    assert tq.lib().tq_ctx_set_decode_path(ctx.handle, 7) == tq.TQ_EINVAL
+    for path in ("simt", "mma", "auto"):
+        ctx.set_decode_path(path)
+        assert ctx.workspace_bytes(2, 8, 2, 700) > 0
+
+
+@pytest.mark.parametrize("path", ["tc", "mma", "simt"])
+def test_decode_long_sequences_each_kernel(path):
+    """Sequences of ~120 pages, so that every CTA of the bit-plane kernels streams far more
+    pages than its shared-memory ring holds (ring refills, many segments), checked on two
+    heads against the oracle on the GPU's own pages."""
+    d, b, G, B, H, maxT = 128, 3, 4, 2, 8, 15360
+    run = P.Run(d, b, B, H, G * H, maxT, decode_path=path)
+    gen = torch.Generator().manual_seed(11)
+    for bb in range(B):   # quantize one sequence at a time to keep host memory small
+        k = (torch.randn(1, H, maxT, d, generator=gen) * 1.3).to(torch.bfloat16)
+        v = torch.randn(1, H, maxT, d, generator=gen).to(torch.bfloat16)
+        run.ctx.quantize_kv(k.cuda(), v.cuda(), torch.zeros(1, dtype=torch.int32, device="cuda"),
+                            run.cache[bb * H * run.n_pages * run.ctx.page_bytes:], maxT)
+    q = torch.randn(B, G * H, d, generator=gen)
+    seq_lens = [maxT, 14001]
+    out, lg = run.decode(q, seq_lens, logits=True)
+    assert run.status() == tq.TQ_OK
+    out, lg = out.cpu().numpy(), lg.cpu().numpy()
+    cache = run.cache_np()
+    for bb, h in [(0, 3), (1, 7)]:
+        T = seq_lens[bb]
+        tok = run.tokens(cache, bb, h, T)
+        for hq in (h * G, h * G + G - 1):
+            o_pages, l_pages = P.oracle_logits_on_pages(run, q[bb, hq].double().numpy(), tok)
+            assert np.max(np.abs(lg[bb, hq, :T] - l_pages)) < P.LOGIT_ATOL
+            assert P.rel_l2(out[bb, hq], o_pages) < P.OUT_ON_PAGES_REL_L2
+    assert np.all(np.isfinite(out))
 
 
 def test_append_one_token_at_a_time_matches_bulk():
