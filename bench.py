@@ -33,9 +33,9 @@ if ROOT not in sys.path:
 
 METRIC = "compressed-KV decode GB/s & % HBM roofline; quantize Mtokens/s (d=128, b=3)"
 UNIT = "GB/s"
-# dram__bytes_read.sum + dram__bytes_write.sum per decode launch, from the ncu capture of
-# the current decode kernels on this workload (None until captured for the current code).
-DECODE_TRAFFIC_BYTES = None
+# dram__bytes_read.sum + dram__bytes_write.sum of one decode_tc_kernel<3,4> launch on this
+# workload (ncu, one launch after warm-up); None whenever that kernel has changed since.
+DECODE_TRAFFIC_BYTES = 461628160
 
 
 def bpt(d, b, m):
@@ -351,7 +351,7 @@ def run_ours(args, w):
         "quantize_ms": t_q,
         "decode_us_per_step": t_dphase / S * 1e3,
         "decode_call_us": t_call * 1e3,
-        "roofline": {"bound": "hbm", "kernel": "tq_attn_decode", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "tq_attn_decode (decode_tc_kernel + prologue + combine)", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": DECODE_TRAFFIC_BYTES, "algorithmic_bytes_per_launch": per_launch_bytes},
         "e2e": {"value": world * dec_bytes / (t_e2e_d * 1e-3) / 1e9, "unit": UNIT,
