@@ -4,27 +4,27 @@
 // the value accumulation are contractions over bit planes of the codes, each plane word
 // turned into e4m3 operands beta_k + gamma_k * bit by one AND-OR (bitplane.h), the per-
 // position scales folded into the other operand.  What changes is where the MMAs run:
-//   A_s (TMEM, lane = token)      key planes and the sign plane of one page, NS x 128 bytes
+//   A_s (smem, K-major, x2)       key planes and the sign plane of one page (row = token),
+//                                 NS x 128 bytes per row
 //   B_s (smem, K-major)           query pieces: 3 e4m3 pieces per head for the key term and
 //                                 3 for the sign term (columns), one row block per plane
-//   D_s (TMEM, lane = token)      score partial sums, read back by the token warps
-//   A_v (TMEM, lane = coordinate) value planes of one page, PV x 128 bytes
-//   B_v (smem, K-major)           softmax weights of the page, 2 e4m3 pieces per head
+//   D_s (TMEM, lane = token, x2)  score partial sums, read back by the token warps
+//   A_v (TMEM, lane = coordinate, x2) value planes of one page, PV x 128 bytes
+//   B_v (smem, K-major, x2)       softmax weights of the page, 2 e4m3 pieces per head
 //   D_v (TMEM, lane = coordinate) one accumulator per value plane, kept across pages
-// One thread issues every MMA (12 instructions for the score of a page at b = 3, 16 for
-// the values) and the tensor pipe runs them asynchronously; completion is signalled on
-// mbarriers by tcgen05.commit.
+// Every per-page operand is double-buffered, so each producer / consumer pair has two pages
+// in flight and hands over once per page: a hand-off costs a few hundred cycles on B300, and
+// chains with one page in flight were what bounded earlier versions of this kernel.
 //
 // Warp roles, 16 warps, handing work over through mbarriers (no CTA barrier per page):
 //   warps 0-3   token warps (TMEM lane = token): read D_s, form logits, run the lazy online
 //               softmax, write B_v and, when the running maximum moves, rescale D_v
-//   warps 4-7   key-plane warps (lane = token): key XOR planes and the sign plane -> A_s
+//   warps 4-7   key-plane warps (row = token): key XOR planes and the sign plane -> A_s
 //   warps 8-11  value-plane warps (lane = coordinate): value XOR planes -> A_v; epilogue
-//   warp 12     issues the score MMAs, warp 13 the value MMAs (one lane each)
-//   warp 14     keeps the page ring filled with cp.async.bulk
-// Each plane has its own ready / done barrier pair, so the planes of page p+1 are stored
-// while the MMAs of page p still read the other planes.  A tcgen05.mma of M = 128, K = 32
-// costs ~47 cycles for any N up to 64 on B300; the 28 MMAs of a page (b = 3) are the floor.
+//   warp 12     issues the score MMAs (12 per page at b = 3), warp 13 the value MMAs (16)
+//   warps 14-15 wait for the operands of the two issuers; warp 15 also refills the page ring
+// A tcgen05.mma of M = 128, K = 32 costs ~46 cycles for any N up to 64 on B300 (two issuing
+// threads overlap to ~38): the 28 MMAs of a page (b = 3) are the floor of this kernel.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -53,6 +53,7 @@ constexpr int kWarpWM = 15;           // waits for the value operands, hands the
 constexpr int kL2Ahead = 12;
 constexpr float kTau = 3.0f;          // lazy-maximum threshold (natural-log units)
 constexpr float kSB = 2.0f;           // e4m3 range scale of the softmax weights
+constexpr int kSmemMax = 227 * 1024;
 
 __host__ __device__ constexpr int rnd(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -65,35 +66,39 @@ struct Cfg {
   static constexpr int NHALF = rnd(3 * GP, 8);         // score columns: [key term | sign term]
   static constexpr int NSC = rnd(2 * NHALF, 16);
   static constexpr int NVC = 2 * GP < 16 ? 16 : 2 * GP;  // value columns: 2 pieces per head
-  // tensor-memory columns: D_s (double-buffered when it fits), D_v, A_s, A_v
+  // tensor memory: D_s (double-buffered when it fits), D_v, A_v (double-buffered)
   static constexpr int DS_COLS = rnd(NSC, 32);
   static constexpr int DV_COLS = rnd(PV * NVC, 32);
-  static constexpr int DSB = 2 * DS_COLS + DV_COLS + (NS + PV) * 32 <= 512 ? 2 : 1;
+  static constexpr int AV_COLS = PV * 32;
+  static constexpr int DSB = 2 * DS_COLS + DV_COLS + 2 * AV_COLS <= 512 ? 2 : 1;
   static constexpr int TD_S = 0;
   static constexpr int TD_V = DSB * DS_COLS;
-  static constexpr int TA_S = TD_V + DV_COLS;
-  static constexpr int TA_V = TA_S + NS * 32;
-  static constexpr int TCOLS = TA_V + PV * 32;
+  static constexpr int TA_V = TD_V + DV_COLS;
+  static constexpr int TCOLS = TA_V + 2 * AV_COLS;
   static constexpr int TALLOC = TCOLS <= 256 ? 256 : 512;
-  // shared memory
+  // shared memory: A_s (key planes, K-major canonical, double-buffered), B_s, B_v (x2), q,
+  // per-head constants, reductions, mbarriers, then as many ring pages as fit (<= 8)
   static constexpr int PAGE = PL::bytes;
-  static constexpr int NBUF = (120 * 1024) / PAGE > 8 ? 8 : (120 * 1024) / PAGE;
+  static constexpr int AS_BYTES = 128 * NS * 128;                // per buffer
   static constexpr int BS_BYTES = NSC * NS * 128;
-  static constexpr int BV_BYTES = NVC * 128;                    // per buffer, 2 buffers
-  static constexpr int OFF_PAGES = 0;
-  static constexpr int OFF_BS = OFF_PAGES + NBUF * PAGE;
+  static constexpr int BV_BYTES = NVC * 128;                     // per buffer
+  static constexpr int OFF_AS = 0;
+  static constexpr int OFF_BS = OFF_AS + 2 * AS_BYTES;
   static constexpr int OFF_BV = OFF_BS + BS_BYTES;
-  static constexpr int OFF_Q = OFF_BV + 2 * BV_BYTES;           // [GP][2][128] f32
-  static constexpr int OFF_HEAD = OFF_Q + GP * 2 * 128 * 4;     // [GP][8] f32
-  static constexpr int OFF_RED = OFF_HEAD + GP * 8 * 4;         // [4 warps][GP + 1][3] f32
-  static constexpr int OFF_F = OFF_RED + 4 * (GP + 1) * 3 * 4;  // n_ref of the segment
+  static constexpr int OFF_Q = OFF_BV + 2 * BV_BYTES;            // [GP][2][128] f32
+  static constexpr int OFF_HEAD = OFF_Q + GP * 2 * 128 * 4;      // [GP][8] f32
+  static constexpr int OFF_RED = OFF_HEAD + GP * 8 * 4;          // [4 warps][GP + 1][3] f32
+  static constexpr int OFF_F = OFF_RED + 4 * (GP + 1) * 3 * 4;   // n_ref of the segment
   static constexpr int OFF_MBAR = rnd(OFF_F + 16, 8);
-  // full[NBUF], empty[NBUF], as_ready[NS], s_pl[NS], ds_free[2], av_ready[PV], v_pl[PV],
-  // bv_ready[2], s_fin[2], v_fin[2], teardown[2]
-  static constexpr int NMBAR = 2 * NBUF + 2 * NS + 2 * PV + 10;
-  static constexpr int OFF_MISC = OFF_MBAR + NMBAR * 8;         // tmem base, fail
-  static constexpr int SMEM = OFF_MISC + 16;
-  static constexpr bool SUPPORTED = TCOLS <= 512 && SMEM <= 225 * 1024 && NBUF >= 4 && NS <= 3 && PV <= 4;
+  // full[8], empty[8], as_ready[2], as_free[2], s_fin[2], ds_free[2], av_ready[2], v_fin[2],
+  // bv_ready[2], teardown[2]
+  static constexpr int NMBAR = 16 + 16;
+  static constexpr int OFF_MISC = OFF_MBAR + NMBAR * 8;          // tmem base, fail
+  static constexpr int OFF_PAGES = rnd(OFF_MISC + 16, 128);
+  static constexpr int NBUF_FIT = (kSmemMax - OFF_PAGES) / PAGE;
+  static constexpr int NBUF = NBUF_FIT > 8 ? 8 : NBUF_FIT;
+  static constexpr int SMEM = OFF_PAGES + NBUF * PAGE;
+  static constexpr bool SUPPORTED = TCOLS <= 512 && SMEM <= kSmemMax && NBUF >= 4;
 };
 
 // OR-vote / barrier among the four token warps (named barrier 1).
@@ -125,30 +130,31 @@ __device__ __forceinline__ void pair_sync(int id) {
 
 // bit position (0..7) of coordinate or token slot x within its plane word
 __host__ __device__ __forceinline__ int kpos_of(int x) { return 2 * (x >> 5) + ((x >> 4) & 1); }
-// coordinate / token slot held by byte e of TMEM column (w * 8 + k) of a plane
+// coordinate / token slot held by byte e of operand column (w * 8 + k) of a plane
 __host__ __device__ __forceinline__ int slot_of_col(int w, int k, int e) {
   return 32 * (k >> 1) + 16 * (k & 1) + 4 * w + e;
 }
 
-// XOR of the code words selected by odd subset `pl`, expanded to 32 e4m3 columns and stored
-// into this warp's lane quarter of a tensor-memory plane.
+// XOR of the code words whose bit is set in `mask` (one odd subset of the code bits).
 template <int NB>
-__device__ __forceinline__ void plane_to_tmem(const uint4 (&w)[NB], int pl, uint32_t taddr) {
-  uint32_t x[4] = {0u, 0u, 0u, 0u};
+__device__ __forceinline__ void xor_planes(const uint4 (&w)[NB], uint32_t mask, uint32_t (&x)[4]) {
+  x[0] = x[1] = x[2] = x[3] = 0u;
 #pragma unroll
-  for (int q = 0; q < NB; ++q)
-    if ((mono_mask16(pl) >> q) & 1) {
-      x[0] ^= w[q].x;
-      x[1] ^= w[q].y;
-      x[2] ^= w[q].z;
-      x[3] ^= w[q].w;
-    }
-  uint32_t r[32];
+  for (int q = 0; q < NB; ++q) {
+    const uint32_t sel = 0u - ((mask >> q) & 1u);
+    x[0] ^= w[q].x & sel;
+    x[1] ^= w[q].y & sel;
+    x[2] ^= w[q].z & sel;
+    x[3] ^= w[q].w & sel;
+  }
+}
+
+// One row of a plane: four plane words expanded to the 32 e4m3 operand words (128 bytes).
+__device__ __forceinline__ void expand_words(const uint32_t (&x)[4], uint32_t (&r)[32]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c)
 #pragma unroll
     for (int k = 0; k < 8; ++k) r[8 * c + k] = expand_at(x[c], k);
-  tmem_st32(taddr, r);
 }
 
 template <int BITS, int GP>
@@ -159,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
   constexpr int NSC = C::NSC, NVC = C::NVC, NHALF = C::NHALF, DSB = C::DSB;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint8_t* s_pages = smem + C::OFF_PAGES;
+  uint8_t* s_as = smem + C::OFF_AS;
   uint8_t* s_bs = smem + C::OFF_BS;
   uint8_t* s_bv = smem + C::OFF_BV;
   float* s_q = reinterpret_cast<float*>(smem + C::OFF_Q);
@@ -166,25 +173,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
   float* s_red = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* s_f = reinterpret_cast<float*>(smem + C::OFF_F);
   uint64_t* mb = reinterpret_cast<uint64_t*>(smem + C::OFF_MBAR);
-  uint64_t* s_full = mb;                   // page in slot landed (loader, + tx bytes)
-  uint64_t* s_empty = mb + NBUF;           // page in slot read by every consumer warp (12)
-  uint64_t* as_ready = mb + 2 * NBUF;      // [NS] key plane stored in A_s (4 key-plane warps)
-  uint64_t* s_pl = as_ready + NS;          // [NS] score MMAs reading key plane done (commit)
-  uint64_t* ds_free = s_pl + NS;           // [2] D_s buffer read by the token warps (4)
-  uint64_t* av_ready = ds_free + 2;        // [PV] value plane stored in A_v (4 value-plane warps)
-  uint64_t* v_pl = av_ready + PV;          // [PV] value MMAs reading value plane done (commit)
-  uint64_t* bv_ready = v_pl + PV;          // [2] B_v buffer written, D_v rescaled (4 token warps)
-  // [2] every score MMA of a page done, one barrier per D_s buffer; [2] every value MMA of a
-  // page done, one barrier per page parity.  Waiting on these keeps each barrier at most one
-  // phase ahead of its waiter, so a parity wait never mistakes an older phase for a newer one.
-  uint64_t* s_fin = bv_ready + 2;
-  uint64_t* v_fin = s_fin + 2;
-  uint64_t* td_bar = v_fin + 2;            // [2] teardown drains of the two MMA issuers
+  // Every hand-off barrier below exists once per buffer (index = page & 1) and completes once
+  // per page of that parity, and every waiter has waited the previous completion: a parity
+  // wait can therefore never mistake an older phase for a newer one.
+  uint64_t* s_full = mb;            // [8]  page in ring slot landed (+ tx bytes)
+  uint64_t* s_empty = mb + 8;       // [8]  page read by every consumer warp (12)
+  uint64_t* as_ready = mb + 16;     // [2]  key planes of the page stored in A_s (4 warps)
+  uint64_t* as_free = mb + 18;      // [2]  score MMAs reading that A_s buffer done (commit)
+  uint64_t* s_fin = mb + 20;        // [2]  score MMAs into that D_s buffer done (commit)
+  uint64_t* ds_free = mb + 22;      // [2]  D_s buffer read by the token warps (4)
+  uint64_t* av_ready = mb + 24;     // [2]  value planes stored in that A_v buffer (4 warps)
+  uint64_t* v_fin = mb + 26;        // [2]  value MMAs of the page done (commit)
+  uint64_t* bv_ready = mb + 28;     // [2]  B_v buffer written, D_v rescaled (4 warps)
+  uint64_t* td_bar = mb + 30;       // [2]  teardown drains of the two MMA issuers
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* s_fail = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = 32 * (warp & 3) + lane;    // TMEM lane of this thread (4-warp roles)
+  const int row = 32 * (warp & 3) + lane;    // TMEM lane / operand row of this thread (4-warp roles)
   const int G = a.group, PM = a.pages_per_seq;
   const float inv_sqrt_d = rsqrtf((float)D);
   const float qjl_c = 1.2533141373155002512f / (float)D;   // sqrt(pi/2) / m, m = d
@@ -195,23 +201,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
 
   if (warp == 0) tmem_alloc(s_tmem, C::TALLOC);
   if (tid == 0) {
-    for (int i = 0; i < NBUF; ++i) {
+    for (int i = 0; i < 8; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 12);
     }
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&as_ready[i], 4);
-      mbar_init(&s_pl[i], 1);
-    }
-    for (int i = 0; i < PV; ++i) {
-      mbar_init(&av_ready[i], 4);
-      mbar_init(&v_pl[i], 1);
-    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ds_free[i], 4);
-      mbar_init(&bv_ready[i], 4);
+      mbar_init(&as_ready[i], 4);
+      mbar_init(&as_free[i], 1);
       mbar_init(&s_fin[i], 1);
+      mbar_init(&ds_free[i], 4);
+      mbar_init(&av_ready[i], 4);
       mbar_init(&v_fin[i], 1);
+      mbar_init(&bv_ready[i], 4);
       mbar_init(&td_bar[i], 1);
     }
     *s_fail = 0;
@@ -229,17 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
   constexpr uint32_t idesc_s = make_idesc(0, 0, 128, NSC);
   constexpr uint32_t idesc_v = make_idesc(0, 0, 128, NVC);
 
-  // every hand-off barrier completes once per page; pages are counted over all segments
   uint32_t pg_base = 0;      // pages (== ring fills) of the previous segments
-  uint32_t issued = 0;       // ring fills issued (loader lane)
+  uint32_t issued = 0;       // ring fills issued (value-waiter lane)
 
   auto fail_now = [&]() {
     if (lane == 0) atomicOr(a.status, kFlagTimeout);
     *s_fail = 1;
   };
-  // bounded wait for the k-th completion (0-based) of a barrier that completes once per use
-  // Once a wait timed out every later wait returns at once: all roles still run their loops
-  // to the end, so the named-barrier counts stay balanced and the kernel finishes.
+  // Bounded wait for the k-th completion (0-based) of a barrier.  Once a wait timed out every
+  // later wait returns at once: all roles still run their loops to the end, so the paired
+  // named-barrier counts stay balanced and the kernel finishes.
   auto wait_k = [&](uint64_t* bar, uint32_t k) {
     if (*s_fail) return;
     if (!mbar_wait(bar, k & 1)) fail_now();
@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
     const int slot = blockIdx.x - (seq * PM) / a.chunk;
     float* rec = a.part + ((size_t)seq * a.slots + slot) * G * (2 + D);
     const uint8_t* seq_base = a.cache + (size_t)seq * PM * PL::bytes;
+    // ring slot / use of the page with segment index p (ring fills are counted over segments)
     auto ring_slot = [&](int p) { return (pg_base + p) % NBUF; };
     auto ring_use = [&](int p) { return (pg_base + p) / NBUF; };
     auto pg_ptr = [&](int p) { return s_pages + ring_slot(p) * C::PAGE; };
@@ -389,48 +390,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
     __syncthreads();
 
 
+
     if (n_pages > 0) {
       if (warp == kWarpWS) {
-        // ============ score waiter: operands of the next plane ready -> meet the score issuer ============
+        // ============ score waiter: A_s(g) stored and D_s buffer free -> meet the score issuer ============
         for (int p = 0; p < n_pages; ++p) {
-          const uint32_t g = pg_base + p, db = DSB == 2 ? (g & 1) : 0;
-#pragma unroll 1
-          for (int pl = 0; pl < NS; ++pl) {
-            wait_k(&as_ready[pl], g);
-            if (pl == 0 && g >= (uint32_t)DSB) wait_k(&ds_free[db], g / DSB - 1);
-            pair_sync(kNbScore);
-          }
+          const uint32_t g = pg_base + p, x = g & 1;
+          wait_k(&as_ready[x], g >> 1);
+          if (DSB == 2 && g >= 2) wait_k(&ds_free[x], (g >> 1) - 1);
+          if (DSB == 1 && g >= 1) wait_k(&ds_free[(g - 1) & 1], (g - 1) >> 1);
+          pair_sync(kNbScore);
         }
       } else if (warp == kWarpS) {
-        // ============ score MMAs: D_s[token][column] = sum over planes of A_s(plane) x B_s ============
+        // ============ score MMAs: D_s[token][column] = A_s[token][plane, coordinate] x B_s ============
         const uint32_t bs = smem_u32(s_bs);
         for (int p = 0; p < n_pages; ++p) {
-          const uint32_t g = pg_base + p, db = DSB == 2 ? (g & 1) : 0;
-#pragma unroll 1
-          for (int pl = 0; pl < NS; ++pl) {
-            pair_sync(kNbScore);
-            if (lane == 0) {
-              tc_fence_after();
+          const uint32_t g = pg_base + p, x = g & 1, db = DSB == 2 ? x : 0;
+          pair_sync(kNbScore);
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t as = smem_u32(s_as + x * C::AS_BYTES);
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                mma_f8_ts(tmem + C::TD_S + db * C::DS_COLS, tmem + C::TA_S + 32 * pl + 8 * ks,
-                          smem_desc(bs + (4 * pl + ks) * 256, 128, NS * 1024), idesc_s, pl > 0 || ks > 0);
-              tc_commit(&s_pl[pl]);
-            }
+            for (int ks = 0; ks < NS * 4; ++ks)
+              mma_f8_ss(tmem + C::TD_S + db * C::DS_COLS, smem_desc(as + ks * 256, 128, NS * 1024),
+                        smem_desc(bs + ks * 256, 128, NS * 1024), idesc_s, ks > 0);
+            tc_commit(&as_free[x]);
+            tc_commit(&s_fin[x]);
           }
-          if (lane == 0) tc_commit(&s_fin[db]);
         }
       } else if (warp == kWarpWM) {
-        // ============ value waiter: operands ready -> meet the value issuer; page ring refills ============
+        // ============ value waiter: A_v(g), B_v(g) ready -> meet the value issuer; ring refills ============
         for (int p = 0; p < n_pages; ++p) {
-          const uint32_t g = pg_base + p;
-          wait_k(&bv_ready[g & 1], g >> 1);
+          const uint32_t g = pg_base + p, x = g & 1;
+          wait_k(&av_ready[x], g >> 1);
+          wait_k(&bv_ready[x], g >> 1);
           pair_sync(kNbValue);
-#pragma unroll 1
-          for (int pl = 0; pl < PV; ++pl) {
-            wait_k(&av_ready[pl], g);
-            pair_sync(kNbValue);
-          }
           // every consumer has read page p by now: its slot takes page p + NBUF
           if (lane == 0 && p + NBUF < n_pages) {
             wait_k(&s_empty[ring_slot(p)], ring_use(p));
@@ -448,27 +442,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
       } else if (warp == kWarpM) {
         // ============ value MMAs: D_v(plane)[coordinate][column] += A_v(plane) x B_v ============
         for (int p = 0; p < n_pages; ++p) {
-          const uint32_t g = pg_base + p;
-          pair_sync(kNbValue);   // B_v(p) written, D_v rescaled
-          const uint32_t bva = smem_u32(s_bv + (g & 1) * C::BV_BYTES);
-#pragma unroll 1
-          for (int pl = 0; pl < PV; ++pl) {
-            pair_sync(kNbValue);
-            if (lane == 0) {
-              tc_fence_after();
+          const uint32_t g = pg_base + p, x = g & 1;
+          pair_sync(kNbValue);
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t bva = smem_u32(s_bv + x * C::BV_BYTES);
+            const uint32_t av = tmem + C::TA_V + x * C::AV_COLS;
+#pragma unroll
+            for (int pl = 0; pl < PV; ++pl)
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
-                mma_f8_ts(tmem + C::TD_V + pl * NVC, tmem + C::TA_V + 32 * pl + 8 * ks,
-                          smem_desc(bva + ks * 256, 128, 1024), idesc_v, !(p == 0 && ks == 0));
-              tc_commit(&v_pl[pl]);
-            }
+                mma_f8_ts(tmem + C::TD_V + pl * NVC, av + 32 * pl + 8 * ks, smem_desc(bva + ks * 256, 128, 1024),
+                          idesc_v, !(p == 0 && ks == 0));
+            tc_commit(&v_fin[x]);
           }
-          if (lane == 0) tc_commit(&v_fin[g & 1]);
         }
       } else if (warp >= 4 && warp < 8) {
-        // ============ key-plane warps (lane = token): XOR planes and the sign plane -> A_s ============
+        // ============ key-plane warps (row = token): XOR planes and the sign plane -> A_s (smem) ============
         for (int p = 0; p < n_pages; ++p) {
-          const uint32_t g = pg_base + p;
+          const uint32_t g = pg_base + p, x = g & 1;
           wait_k(&s_full[ring_slot(p)], ring_use(p));
           const uint8_t* pgp = pg_ptr(p);
           uint4 wk[BK + 1];
@@ -478,26 +470,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           wk[BK] = *reinterpret_cast<const uint4*>(pgp + PL::off_signs + (size_t)row * 16);
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
-#pragma unroll
+          if (g >= 2) wait_k(&as_free[x], (g >> 1) - 1);   // the score MMAs of page g-2 are done
+          uint8_t* as = s_as + x * C::AS_BYTES;
+#pragma unroll 1
           for (int pl = 0; pl < NS; ++pl) {
-            if (g > 0) wait_k(&s_pl[pl], g - 1);   // the previous page's MMAs on this plane are done
-            tc_fence_after();
+            uint32_t x[4];
             if (pl < PK) {
-              plane_to_tmem<BK>(reinterpret_cast<const uint4(&)[BK]>(wk), pl, tl + C::TA_S + 32 * pl);
+              xor_planes<BK + 1>(wk, mono_mask16(pl), x);
             } else {
-              const uint4 ws1[1] = {wk[BK]};
-              plane_to_tmem<1>(ws1, 0, tl + C::TA_S + 32 * pl);
+              x[0] = wk[BK].x;
+              x[1] = wk[BK].y;
+              x[2] = wk[BK].z;
+              x[3] = wk[BK].w;
             }
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&as_ready[pl]);
+            uint32_t r[32];
+            expand_words(x, r);
+            uint8_t* dst = as + canon_off(row, pl * 128, NS * 128);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(dst + j * 128) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
           }
+          fence_proxy_async();   // A_s is read by the tensor cores
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&as_ready[x]);
         }
       } else if (warp >= 8 && warp < 12) {
-        // ============ value-plane warps (lane = coordinate): XOR planes -> A_v ============
+        // ============ value-plane warps (lane = coordinate): XOR planes -> A_v (tensor memory) ============
         for (int p = 0; p < n_pages; ++p) {
-          const uint32_t g = pg_base + p;
+          const uint32_t g = pg_base + p, x = g & 1;
           wait_k(&s_full[ring_slot(p)], ring_use(p));
           const uint8_t* pgp = pg_ptr(p);
           uint4 wv[BV];
@@ -506,16 +506,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
             wv[q] = *reinterpret_cast<const uint4*>(pgp + PL::off_vcodes + ((size_t)q * D + row) * 16);
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
-#pragma unroll
+          if (g >= 2) wait_k(&v_fin[x], (g >> 1) - 1);   // the value MMAs of page g-2 are done
+          tc_fence_after();
+#pragma unroll 1
           for (int pl = 0; pl < PV; ++pl) {
-            if (g > 0) wait_k(&v_pl[pl], g - 1);
-            tc_fence_after();
-            plane_to_tmem<BV>(wv, pl, tl + C::TA_V + 32 * pl);
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&av_ready[pl]);
+            uint32_t xw[4], r[32];
+            xor_planes<BV>(wv, mono_mask16(pl), xw);
+            expand_words(xw, r);
+            tmem_st32(tl + C::TA_V + x * C::AV_COLS + 32 * pl, r);
           }
+          tc_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&av_ready[x]);
         }
       } else if (warp < 4) {
         // ============ token warps (lane = token): logits, lazy softmax, weight operand ============
@@ -527,10 +530,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
         }
         float n_ref = 0.f;
         for (int p = 0; p < n_pages; ++p) {
-          const uint32_t g = pg_base + p, db = DSB == 2 ? (g & 1) : 0;
+          const uint32_t g = pg_base + p, x = g & 1, db = DSB == 2 ? x : 0;
           const uint8_t* pgp = pg_ptr(p);
           wait_k(&s_full[ring_slot(p)], ring_use(p));
-          wait_k(&s_fin[db], DSB == 2 ? g >> 1 : g);   // every score MMA of page p is done
+          const int nvalid = min(128, seq_len - (p_lo + p) * 128);
+          const bool valid = row < nvalid;
+          const float nk = valid ? reinterpret_cast<const float*>(pgp + PL::off_nk)[row] : 0.f;
+          const float gmv = valid ? reinterpret_cast<const float*>(pgp + PL::off_gamma)[row] : 0.f;
+          const float nvt = valid ? reinterpret_cast<const float*>(pgp + PL::off_nv)[row] : 0.f;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
+          wait_k(&s_fin[x], g >> 1);        // every score MMA of page p is done
           tc_fence_after();
           float ds[NSC];
 #pragma unroll
@@ -543,14 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&ds_free[db]);
-          const int nvalid = min(128, seq_len - (p_lo + p) * 128);
-          const bool valid = row < nvalid;
-          const float nk = valid ? reinterpret_cast<const float*>(pgp + PL::off_nk)[row] : 0.f;
-          const float gmv = valid ? reinterpret_cast<const float*>(pgp + PL::off_gamma)[row] : 0.f;
-          const float nvt = valid ? reinterpret_cast<const float*>(pgp + PL::off_nv)[row] : 0.f;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
+          if (lane == 0) mbar_arrive(&ds_free[x]);
           float lg[GP];
           int ovf = nvt > n_ref;
 #pragma unroll
