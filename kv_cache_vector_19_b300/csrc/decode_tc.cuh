@@ -135,18 +135,36 @@ __host__ __device__ __forceinline__ int slot_of_col(int w, int k, int e) {
   return 32 * (k >> 1) + 16 * (k & 1) + 4 * w + e;
 }
 
-// XOR of the code words whose bit is set in `mask` (one odd subset of the code bits).
-template <int NB>
-__device__ __forceinline__ void xor_planes(const uint4 (&w)[NB], uint32_t mask, uint32_t (&x)[4]) {
-  x[0] = x[1] = x[2] = x[3] = 0u;
+// The words of every odd-subset ("monomial") plane of a slot row, built once per page with
+// the subset masks folded at compile time: xp[pl] = XOR of w[q] over the bits q of subset pl.
+template <int NB, int NP>
+__device__ __forceinline__ void monomial_words(const uint4 (&w)[NB], uint4 (&xp)[NP]) {
 #pragma unroll
-  for (int q = 0; q < NB; ++q) {
-    const uint32_t sel = 0u - ((mask >> q) & 1u);
-    x[0] ^= w[q].x & sel;
-    x[1] ^= w[q].y & sel;
-    x[2] ^= w[q].z & sel;
-    x[3] ^= w[q].w & sel;
+  for (int pl = 0; pl < NP; ++pl) {
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int q = 0; q < NB; ++q)
+      if ((mono_mask16(pl) >> q) & 1) {
+        x.x ^= w[q].x;
+        x.y ^= w[q].y;
+        x.z ^= w[q].z;
+        x.w ^= w[q].w;
+      }
+    xp[pl] = x;
   }
+}
+
+// xp[pl] for a runtime plane index (predicated selects; keeps the plane loop rolled).
+template <int NP>
+__device__ __forceinline__ void pick_plane(const uint4 (&xp)[NP], int pl, uint32_t (&x)[4]) {
+  uint4 v = xp[0];
+#pragma unroll
+  for (int i = 1; i < NP; ++i)
+    if (pl == i) v = xp[i];
+  x[0] = v.x;
+  x[1] = v.y;
+  x[2] = v.z;
+  x[3] = v.w;
 }
 
 // One row of a plane: four plane words expanded to the 32 e4m3 operand words (128 bytes).
@@ -380,12 +398,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
     fence_proxy_async();   // B_s is read by the tensor cores
     __syncthreads();
 
-    // token-warp form of the per-head constants: 1/s_k, 1/s_q, C_k, C_q, asum_k * sum q~, sum q_s
+    // token-warp form of the per-head constants.  From the set-up values s_k, s_q (operand
+    // scales), C_k, C_q (beta-term constants), sum q~ and sum q_s:
+    //   <q~, c[idx]> = (mse - C_k) / s_k - asum_k sum q~,  <q_s, 2 sigma - 1> = (qjl - C_q) / s_q - sum q_s,
+    //   logit = (n_k <q~, c[idx]> + gamma sqrt(pi/2)/m <q_s, 2 sigma - 1>) / sqrt(d)
+    //         = n_k (mse ak + bk) + gamma (qjl aq + bq).
     for (int hh = tid; hh < GP; hh += kThreads) {
       float* hp = s_head + hh * 8;
-      hp[0] = 1.f / hp[0];
-      hp[1] = 1.f / hp[1];
-      hp[4] = a.asum_k * hp[4];
+      const float sk = hp[0], sq = hp[1], ck = hp[2], cq = hp[3], sumk = hp[4], sumq = hp[5];
+      hp[0] = inv_sqrt_d / sk;
+      hp[1] = (-ck / sk - a.asum_k * sumk) * inv_sqrt_d;
+      hp[2] = qjl_c * inv_sqrt_d / sq;
+      hp[3] = (-cq / sq - sumq) * qjl_c * inv_sqrt_d;
     }
     __syncthreads();
 
@@ -472,17 +496,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
           if (g >= 2) wait_k(&as_free[x], (g >> 1) - 1);   // the score MMAs of page g-2 are done
           uint8_t* as = s_as + x * C::AS_BYTES;
+          uint4 xk[NS];   // key monomial planes, then the sign plane
+          {
+            uint4 kp[PK];
+            monomial_words<BK + 1, PK>(wk, kp);
+#pragma unroll
+            for (int i = 0; i < PK; ++i) xk[i] = kp[i];
+            xk[PK] = wk[BK];
+          }
 #pragma unroll 1
           for (int pl = 0; pl < NS; ++pl) {
             uint32_t x[4];
-            if (pl < PK) {
-              xor_planes<BK + 1>(wk, mono_mask16(pl), x);
-            } else {
-              x[0] = wk[BK].x;
-              x[1] = wk[BK].y;
-              x[2] = wk[BK].z;
-              x[3] = wk[BK].w;
-            }
+            pick_plane<NS>(xk, pl, x);
             uint32_t r[32];
             expand_words(x, r);
             uint8_t* dst = as + canon_off(row, pl * 128, NS * 128);
@@ -508,10 +533,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
           if (g >= 2) wait_k(&v_fin[x], (g >> 1) - 1);   // the value MMAs of page g-2 are done
           tc_fence_after();
+          uint4 xvp[PV];
+          monomial_words<BV, PV>(wv, xvp);
 #pragma unroll 1
           for (int pl = 0; pl < PV; ++pl) {
             uint32_t xw[4], r[32];
-            xor_planes<BV>(wv, mono_mask16(pl), xw);
+            pick_plane<PV>(xvp, pl, xw);
             expand_words(xw, r);
             tmem_st32(tl + C::TA_V + x * C::AV_COLS + 32 * pl, r);
           }
@@ -558,12 +585,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           int ovf = nvt > n_ref;
 #pragma unroll
           for (int h = 0; h < GP; ++h) {
-            const float* hp = s_head + h * 8;   // 1/s_k, 1/s_q, C_k, C_q, asum_k * sum q~, sum q_s
-            const float mse = ds[3 * h] + 0.0625f * ds[3 * h + 1] + 0.00390625f * ds[3 * h + 2];
-            const float qjl = ds[NHALF + 3 * h] + 0.0625f * ds[NHALF + 3 * h + 1] + 0.00390625f * ds[NHALF + 3 * h + 2];
-            const float dk = fmaf(mse - hp[2], hp[0], -hp[4]);
-            const float dq = fmaf(qjl - hp[3], hp[1], -hp[5]);
-            const float l = fmaf(nk, dk, gmv * qjl_c * dq) * inv_sqrt_d;
+            // folded per-head constants (set-up): logit = nk (mse ak + bk) + gamma (qjl aq + bq)
+            const float4 hc = *reinterpret_cast<const float4*>(s_head + h * 8);
+            const float mse = fmaf(0.00390625f, ds[3 * h + 2], fmaf(0.0625f, ds[3 * h + 1], ds[3 * h]));
+            const float qjl = fmaf(0.00390625f, ds[NHALF + 3 * h + 2], fmaf(0.0625f, ds[NHALF + 3 * h + 1], ds[NHALF + 3 * h]));
+            const float l = fmaf(nk, fmaf(mse, hc.x, hc.y), gmv * fmaf(qjl, hc.z, hc.w));
             lg[h] = (valid && h < G) ? l : -INFINITY;
             if (a.logits && valid && h < G)
               a.logits[((size_t)b * a.q_heads + (size_t)kvh * G + h) * a.max_tokens + (size_t)(p_lo + p) * 128 + row] = l;
@@ -624,19 +650,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           uint32_t wb[NVC / 4];
 #pragma unroll
           for (int i = 0; i < NVC / 4; ++i) wb[i] = 0u;
+          // two heads per conversion: word h/2 holds rows 2h..2h+3 = [hi(h), lo(h), hi(h+1), lo(h+1)]
 #pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            const float pr = lg[h] == -INFINITY ? 0.f : __expf(lg[h] - m_run[h]);
-            l_part[h] += pr;
-            const float x = pr * xs;
-            const uint32_t hi = cvt_e4m3x2(0.f, x) & 0xFF;
-            const float hf = e4m3x2_to_f2(hi).x;
-            const uint32_t lo = cvt_e4m3x2(0.f, 16.f * (x - hf)) & 0xFF;
-            const float bsum = hf + 0.0625f * e4m3x2_to_f2(lo).x;
-            c_part[h] += v_beta * bsum;
-            g_part[h] += v_gamma * bsum;
-            wb[(2 * h) >> 2] |= hi << (8 * ((2 * h) & 3));
-            wb[(2 * h + 1) >> 2] |= lo << (8 * ((2 * h + 1) & 3));
+          for (int h = 0; h < GP; h += 2) {
+            const float p0 = lg[h] == -INFINITY ? 0.f : __expf(lg[h] - m_run[h]);
+            const float p1 = lg[h + 1] == -INFINITY ? 0.f : __expf(lg[h + 1] - m_run[h + 1]);
+            l_part[h] += p0;
+            l_part[h + 1] += p1;
+            const float x0 = p0 * xs, x1 = p1 * xs;
+            const uint32_t hi2 = cvt_e4m3x2(x1, x0);
+            const float2 hf = e4m3x2_to_f2(hi2);
+            const uint32_t lo2 = cvt_e4m3x2(16.f * (x1 - hf.y), 16.f * (x0 - hf.x));
+            const float2 lf = e4m3x2_to_f2(lo2);
+            const float b0 = fmaf(0.0625f, lf.x, hf.x), b1 = fmaf(0.0625f, lf.y, hf.y);
+            c_part[h] = fmaf(v_beta, b0, c_part[h]);
+            c_part[h + 1] = fmaf(v_beta, b1, c_part[h + 1]);
+            g_part[h] = fmaf(v_gamma, b0, g_part[h]);
+            g_part[h + 1] = fmaf(v_gamma, b1, g_part[h + 1]);
+            wb[h >> 1] = __byte_perm(hi2, lo2, 0x5140);
           }
           // B_v buffer of page p: its previous user, the value MMA of page p-2, must be done
           if (p >= 2) wait_k(&v_fin[g & 1], (g >> 1) - 1);
