@@ -375,7 +375,9 @@ def run_ours(args, w):
 
 
 def run_sweep(args):
-    """Throughput per (d, b) point of the bit/dim sweep (1 KV head, 65,536 tokens, 16 queries)."""
+    """Per (d, b) point of the bit/dim sweep (1 KV head, 65,536 tokens, 16 queries): quantize
+    Mtokens/s, decode us and GB/s, normalized reconstruction MSE of keys and values (from
+    tq_dequantize_kv) and the bias / RMS of the inner-product error <q, k^> - <q, k>."""
     import torch
 
     import kv_cache_vector_19_b300 as tq
@@ -410,10 +412,27 @@ def run_sweep(args):
             tq_ms = e[0].elapsed_time(e[1]) / args.steps
             td_ms = e[1].elapsed_time(e[2]) / args.steps
             nbytes = T * bpt(d, b, d)
+            # reconstruction and inner-product error of the cached vectors (tq_dequantize_kv)
+            khat = torch.empty(1, 1, T, d, device="cuda")
+            vhat = torch.empty(1, 1, T, d, device="cuda")
+            ctx.dequantize_kv(cache, zero, 1, 1, T, T, khat, vhat)
+            kx, vx = k[0, 0].float(), v[0, 0].float()
+            kh, vh = khat[0, 0], vhat[0, 0]
+            nmse_k = ((kh - kx).pow(2).sum(-1) / kx.pow(2).sum(-1).clamp_min(1e-30)).mean().item()
+            nmse_v = ((vh - vx).pow(2).sum(-1) / vx.pow(2).sum(-1).clamp_min(1e-30)).mean().item()
+            qq = q[0].float()                      # [nq, d]
+            exact = kx @ qq.t()                    # <q, k> for every token and query
+            err = kh @ qq.t() - exact
+            st = ctx.device_status()
+            if st != tq.TQ_OK:
+                raise SystemExit(f"device status in sweep d={d} b={b}: {tq.tq_status_string(st)}")
             print(json.dumps({"sweep_point": f"d{d}_b{b}", "head_dim": d, "bits": b, "tokens": T,
                               "queries": nq, "quantize_mtok_s": T / tq_ms / 1e3, "decode_us": td_ms * 1e3,
                               "decode_gbs": nbytes / td_ms / 1e6, "compressed_bytes": nbytes,
-                              "bytes_per_token": bpt(d, b, d), "compression_vs_bf16": 4 * d / bpt(d, b, d)}),
+                              "bytes_per_token": bpt(d, b, d), "compression_vs_bf16": 4 * d / bpt(d, b, d),
+                              "recon_nmse_k": nmse_k, "recon_nmse_v": nmse_v,
+                              "ip_bias": err.mean().item(), "ip_rms": err.pow(2).mean().sqrt().item(),
+                              "ip_rms_rel": (err.pow(2).mean() / exact.pow(2).mean()).sqrt().item()}),
                   flush=True)
             ctx.close()
     return 0

@@ -195,6 +195,20 @@ int tq_attn_decode_noalloc(const tq_ctx* ctx, const float* q, int batch, int q_h
                            const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
                            float* logits_out, void* stream);
 
+/* Reconstructs cached vectors in the original frame, from the page contents alone
+ * ([BLOG] 1.2: dequantization of stage 1, x~ = n Pi^T c[idx], and the stage-2 estimate of the
+ * key residual from its signs; [3BITS] "Python + HuggingFace": dequantize(indices, norms)):
+ *   keys    k^ = n_k Pi^T c_K[idx] + gamma sqrt(pi/2)/m S^T (2 sigma - 1)
+ *   values  v^ = n_v Pi^T c_V[idx]
+ *   cache      as written by tq_quantize_kv
+ *   start_pos  device int32 [batch]: slot of the first vector read for each sequence
+ *   k_out, v_out  device fp32 [batch][kv_heads][n_tokens][d], either may be NULL (skipped)
+ * A sequence whose start_pos[b] < 0 or start_pos[b] + n_tokens > max_tokens is skipped and
+ * sets the sticky TQ_EBOUNDS flag.  Not on the decode path (which never materialises k^ or
+ * v^): for inspection, error statistics and tests.  CUDA cores, fp32. */
+int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch, int kv_heads, int max_tokens,
+                     const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream);
+
 /* Synchronises `stream`, then returns and clears the sticky device status: TQ_OK,
  * TQ_EBOUNDS or TQ_ETIMEOUT. */
 int tq_get_device_status(const tq_ctx* ctx, void* stream);

@@ -52,6 +52,7 @@ _SIGS = {
     "tq_attn_decode": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp,
                                 _c_size, _vp]),
     "tq_attn_decode_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp]),
+    "tq_dequantize_kv": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp]),
     "tq_get_device_status": (_c_int, [_vp, _vp]),
     "tq_status_string": (ctypes.c_char_p, [_c_int]),
 }
@@ -256,6 +257,13 @@ class Context:
         rc = tq_quantize_kv(self._ctx, _ptr(k), _ptr(v), B, H, N, _ptr(start_pos), _ptr(cache), max_tokens,
                             _stream_handle(stream))
         _check("tq_quantize_kv", rc)
+
+    def dequantize_kv(self, cache, start_pos, batch, kv_heads, n_tokens, max_tokens, k_out=None, v_out=None,
+                      stream=None):
+        """Reconstructed keys / values (fp32 [B, Hkv, n_tokens, d]) of the slots from start_pos[b]."""
+        rc = lib().tq_dequantize_kv(self._ctx, _ptr(cache), batch, kv_heads, max_tokens, _ptr(start_pos), n_tokens,
+                                    _ptr(k_out), _ptr(v_out), _stream_handle(stream))
+        _check("tq_dequantize_kv", rc)
 
     def attn_decode(self, q, cache, seq_lens, kv_heads, max_tokens, out, workspace, logits=None, stream=None):
         """q, out: fp32 [B, Hq, d]; seq_lens: int32 [B] on the device; logits: None or

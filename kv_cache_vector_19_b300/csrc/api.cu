@@ -88,8 +88,8 @@ void release(tq_ctx* c) {
   int prev = -1;
   cudaGetDevice(&prev);
   cudaSetDevice(c->device);
-  float* bufs[] = {c->d_pi, c->d_pit, c->d_st, c->d_spt, c->d_ck, c->d_tk, c->d_cv, c->d_tv, c->d_alpha_k,
-                   c->d_alpha_v};
+  float* bufs[] = {c->d_pi, c->d_pit, c->d_st, c->d_spt, c->d_s, c->d_ck, c->d_tk, c->d_cv, c->d_tv,
+                   c->d_alpha_k, c->d_alpha_v};
   for (float* p : bufs)
     if (p) cudaFree(p);
   if (c->d_status) cudaFree(c->d_status);
@@ -158,6 +158,7 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
     if (rc == TQ_OK) rc = upload(pit, &c->d_pit);
     if (rc == TQ_OK) rc = upload(st, &c->d_st);
     if (rc == TQ_OK) rc = upload(spt, &c->d_spt);
+    if (rc == TQ_OK) rc = upload(c->s, &c->d_s);
     if (rc == TQ_OK) rc = upload(c->ck, &c->d_ck);
     if (rc == TQ_OK) rc = upload(c->tk, &c->d_tk);
     if (rc == TQ_OK) rc = upload(c->cv, &c->d_cv);
@@ -326,6 +327,18 @@ extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int 
                                  workspace, stream);
   return launch_decode_simt(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
                             workspace, stream);
+}
+
+extern "C" int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch, int kv_heads, int max_tokens,
+                                const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream) {
+  if (!ctx) return TQ_EINVAL;
+  if (batch < 1 || kv_heads < 1 || n_tokens < 0 || max_tokens < 1) return TQ_EINVAL;
+  if (batch > 65535 || kv_heads > 65535 || n_tokens > max_tokens) return TQ_EINVAL;
+  if (n_tokens == 0 || (!k_out && !v_out)) return TQ_OK;
+  if (!cache || !start_pos || !aligned(cache, 256) || !aligned(start_pos, 4)) return TQ_EINVAL;
+  if ((k_out && !aligned(k_out, 4)) || (v_out && !aligned(v_out, 4))) return TQ_EINVAL;
+  DeviceGuard guard(ctx->device);
+  return tq::launch_dequantize(ctx, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, stream);
 }
 
 extern "C" int tq_get_device_status(const tq_ctx* ctx, void* stream) {

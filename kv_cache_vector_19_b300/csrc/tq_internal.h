@@ -50,6 +50,7 @@ struct tq_ctx {
   float* d_pit = nullptr;   // [d][d]  Pi^T
   float* d_st = nullptr;    // [d][m]  S^T
   float* d_spt = nullptr;   // [d][m]  (S Pi^T)^T
+  float* d_s = nullptr;     // [m][d]  S, row-major
   float* d_ck = nullptr;    // [lk]
   float* d_tk = nullptr;    // [lk-1]
   float* d_cv = nullptr;    // [lv]
@@ -71,6 +72,8 @@ struct tq_ctx {
 int prepare_quantize_simt(const tq_ctx* ctx);
 namespace tq {
 int prepare_quantize_tc(const tq_ctx* c);
+int launch_dequantize(const tq_ctx* c, const void* cache, int batch, int kv_heads, int max_tokens,
+                      const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream);
 int launch_quantize_tc(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
                        const int32_t* start_pos, void* cache, int max_tokens, void* stream);
 }  // namespace tq
