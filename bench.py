@@ -101,6 +101,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(times_ms, world, device):
+    """Each timing as the maximum over the ranks (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return list(times_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(times_ms), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_gbs(world, bytes_per_rank, t_ms):
+    """Whole-job GB/s: every rank processes bytes_per_rank of its own sequences (replicas) in
+    the max-over-ranks time t_ms."""
+    return world * bytes_per_rank / (t_ms * 1e-3) / 1e9
+
+
 def cpu_oracle_sample(w, seconds=12.0, reps_max=1000):
     """The oracle's own decode over packed pages (unpack + route A for the G query heads
     of one KV head) on a 1024-token sample of the workload, repeated for ~`seconds`.
@@ -327,11 +344,9 @@ def run_ours(args, w):
     mean = lambda xs: sum(xs) / len(xs)
     t_dphase, t_q, t_call = mean(dphase_ms), mean(q_ms), mean(dcall_ms)
     t_e2e_d, t_e2e_q = mean(e2e_d), mean(e2e_q)
-    if world > 1:
-        t = torch.tensor([t_dphase, t_q, t_call, total_ms, t_e2e_d, t_e2e_q], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_dphase, t_q, t_call, total_ms, t_e2e_d, t_e2e_q = t.tolist()
-    value = world * dec_bytes / (t_dphase * 1e-3) / 1e9
+    t_dphase, t_q, t_call, total_ms, t_e2e_d, t_e2e_q = max_over_ranks(
+        [t_dphase, t_q, t_call, total_ms, t_e2e_d, t_e2e_q], world, dev)
+    value = job_gbs(world, dec_bytes, t_dphase)
     peak, peak_kind = read_peaks()
     achieved = per_launch_bytes / (t_call * 1e-3) / 1e9
     h2d = (h_k.numel() + h_v.numel()) * 2 + h_q.numel() * 4 + ((h_kn.numel() + h_vn.numel()) * 2 if appends else 0)
@@ -354,7 +369,7 @@ def run_ours(args, w):
         "roofline": {"bound": "hbm", "kernel": "tq_attn_decode (decode_tc_kernel + prologue + combine)", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": DECODE_TRAFFIC_BYTES, "algorithmic_bytes_per_launch": per_launch_bytes},
-        "e2e": {"value": world * dec_bytes / (t_e2e_d * 1e-3) / 1e9, "unit": UNIT,
+        "e2e": {"value": job_gbs(world, dec_bytes, t_e2e_d), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": t_e2e_q + t_e2e_d,
                 "quantize_mtok_s": world * B * T / (t_e2e_q * 1e-3) / 1e6},

@@ -53,6 +53,11 @@ constexpr int kWarpWM = 15;           // waits for the value operands, hands the
 constexpr int kL2Ahead = 12;
 constexpr float kTau = 3.0f;          // lazy-maximum threshold (natural-log units)
 constexpr float kSB = 2.0f;           // e4m3 range scale of the softmax weights
+// The value accumulator D_v restarts every kFlush pages after the token warps add it into
+// D_acc in fp32: the tensor core's accumulation rounds at a coarser grain than fp32, and over
+// 10^3 pages (the beta offsets of the bit-plane operands keep D_v large) that rounding
+// reached 1e-2 of the output; over 16 pages it stays near 1e-5.
+constexpr int kFlush = 16;
 constexpr int kSmemMax = 227 * 1024;
 
 __host__ __device__ constexpr int rnd(int x, int m) { return (x + m - 1) / m * m; }
@@ -63,18 +68,23 @@ struct Cfg {
   using PL = PageLayout<128, BITS>;
   static constexpr int BK = BITS - 1, BV = BITS;
   static constexpr int PK = 1 << (BK - 1), PV = 1 << (BV - 1), NS = PK + 1;
-  static constexpr int NHALF = rnd(3 * GP, 8);         // score columns: [key term | sign term]
+  static constexpr int NQP = 4;                          // e4m3 pieces per query coordinate
+  static constexpr int NHALF = rnd(NQP * GP, 8);       // score columns: [key term | sign term]
   static constexpr int NSC = rnd(2 * NHALF, 16);
-  static constexpr int NVC = 2 * GP < 16 ? 16 : 2 * GP;  // value columns: 2 pieces per head
-  // tensor memory: D_s (double-buffered when it fits), D_v, A_v (double-buffered)
+  static constexpr int NPW = 2;                           // e4m3 pieces per softmax weight
+  static constexpr int NVC = NPW * GP < 16 ? 16 : NPW * GP;  // value columns: hi, lo per head
+  // tensor memory: D_s (x2 when it fits), D_v (this stretch of pages), D_acc (fp32 total of
+  // the flushed stretches), A_v (x2 when it fits)
   static constexpr int DS_COLS = rnd(NSC, 32);
   static constexpr int DV_COLS = rnd(PV * NVC, 32);
   static constexpr int AV_COLS = PV * 32;
-  static constexpr int DSB = 2 * DS_COLS + DV_COLS + 2 * AV_COLS <= 512 ? 2 : 1;
+  static constexpr int DSB = 2 * DS_COLS + 2 * DV_COLS + 2 * AV_COLS <= 512 ? 2 : 1;
+  static constexpr int AVB = DSB * DS_COLS + 2 * DV_COLS + 2 * AV_COLS <= 512 ? 2 : 1;
   static constexpr int TD_S = 0;
   static constexpr int TD_V = DSB * DS_COLS;
-  static constexpr int TA_V = TD_V + DV_COLS;
-  static constexpr int TCOLS = TA_V + 2 * AV_COLS;
+  static constexpr int TD_ACC = TD_V + DV_COLS;
+  static constexpr int TA_V = TD_ACC + DV_COLS;
+  static constexpr int TCOLS = TA_V + AVB * AV_COLS;
   static constexpr int TALLOC = TCOLS <= 256 ? 256 : 512;
   // shared memory: A_s (key planes, K-major canonical, double-buffered), B_s, B_v (x2), q,
   // per-head constants, reductions, mbarriers, then as many ring pages as fit (<= 8)
@@ -180,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
   using C = Cfg<BITS, GP>;
   using PL = typename C::PL;
   constexpr int D = 128, NS = C::NS, PK = C::PK, PV = C::PV, BK = C::BK, BV = C::BV, NBUF = C::NBUF;
-  constexpr int NSC = C::NSC, NVC = C::NVC, NHALF = C::NHALF, DSB = C::DSB;
+  constexpr int NSC = C::NSC, NVC = C::NVC, NHALF = C::NHALF, DSB = C::DSB, NPW = C::NPW, AVB = C::AVB;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint8_t* s_pages = smem + C::OFF_PAGES;
   uint8_t* s_as = smem + C::OFF_AS;
@@ -334,16 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
     }
     __syncthreads();
     // B_s[n][k], K-major canonical: k = plane * 128 + 4 * (8 w + kpos) + e <-> coordinate
-    // slot_of_col(w, kpos, e); n = 3 h + piece (key term) or NHALF + 3 h + piece (sign term)
+    // slot_of_col(w, kpos, e); n = 4 h + piece (key term) or NHALF + 4 h + piece (sign term)
     for (int e4 = tid; e4 < NSC * NS * 32; e4 += kThreads) {
       const int n = e4 / (NS * 32), kw = e4 % (NS * 32);   // kw = 4-byte group index along K
       const int pl = kw / 32, col = kw % 32, w = col >> 3, kp = col & 7;
       int hh = -1, piece = 0;
       if (n < NHALF) {
-        if (pl < PK) { hh = n / 3; piece = n % 3; }
+        if (pl < PK) { hh = n / 4; piece = n % 4; }
       } else if (pl == PK) {
-        hh = (n - NHALF) / 3;
-        piece = (n - NHALF) % 3;
+        hh = (n - NHALF) / 4;
+        piece = (n - NHALF) % 4;
       }
       uint32_t word = 0u;
       if (hh >= 0 && hh < G) {
@@ -354,9 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
         const float ig = 1.f / e4m3_gamma(kp);
 #pragma unroll
         for (int el = 0; el < 4; ++el) {
-          uint32_t p0, p1, p2;
-          split3(coef * qv[slot_of_col(w, kp, el)] * sc * ig, p0, p1, p2);
-          word |= (piece == 0 ? p0 : piece == 1 ? p1 : p2) << (8 * el);
+          uint32_t pc[4];
+          split4(coef * qv[slot_of_col(w, kp, el)] * sc * ig, pc);
+          word |= (piece == 0 ? pc[0] : piece == 1 ? pc[1] : piece == 2 ? pc[2] : pc[3]) << (8 * el);
         }
       }
       *reinterpret_cast<uint32_t*>(s_bs + canon_off(n, 4 * kw, NS * 128)) = word;
@@ -372,13 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           sk += qk;
           sq += qq;
           for (int pl = 0; pl < PK; ++pl) {
-            uint32_t p0, p1, p2;
-            split3(2.f * a.alpha_k[pl] * qk * sck * ig, p0, p1, p2);
-            cmv += beta * split3_val(p0, p1, p2);
+            uint32_t pc[4];
+            split4(2.f * a.alpha_k[pl] * qk * sck * ig, pc);
+            cmv += beta * split4_val(pc);
           }
-          uint32_t p0, p1, p2;
-          split3(2.f * qq * scq * ig, p0, p1, p2);
-          cqv += beta * split3_val(p0, p1, p2);
+          uint32_t pc[4];
+          split4(2.f * qq * scq * ig, pc);
+          cqv += beta * split4_val(pc);
         }
       }
 #pragma unroll
@@ -471,13 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           if (lane == 0) {
             tc_fence_after();
             const uint32_t bva = smem_u32(s_bv + x * C::BV_BYTES);
-            const uint32_t av = tmem + C::TA_V + x * C::AV_COLS;
+            const uint32_t av = tmem + C::TA_V + (AVB == 2 ? x : 0) * C::AV_COLS;
+            const bool restart = p % kFlush == 0;   // D_v was flushed into D_acc (or the segment starts)
 #pragma unroll
             for (int pl = 0; pl < PV; ++pl)
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
                 mma_f8_ts(tmem + C::TD_V + pl * NVC, av + 32 * pl + 8 * ks, smem_desc(bva + ks * 256, 128, 1024),
-                          idesc_v, !(p == 0 && ks == 0));
+                          idesc_v, !(restart && ks == 0));
             tc_commit(&v_fin[x]);
           }
         }
@@ -531,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
             wv[q] = *reinterpret_cast<const uint4*>(pgp + PL::off_vcodes + ((size_t)q * D + row) * 16);
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
-          if (g >= 2) wait_k(&v_fin[x], (g >> 1) - 1);   // the value MMAs of page g-2 are done
+          if (g >= (uint32_t)AVB) wait_k(&v_fin[(g - AVB) & 1], (g - AVB) >> 1);   // A_v buffer free
           tc_fence_after();
           uint4 xvp[PV];
           monomial_words<BV, PV>(wv, xvp);
@@ -540,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
             uint32_t xw[4], r[32];
             pick_plane<PV>(xvp, pl, xw);
             expand_words(xw, r);
-            tmem_st32(tl + C::TA_V + x * C::AV_COLS + 32 * pl, r);
+            tmem_st32(tl + C::TA_V + (AVB == 2 ? x : 0) * C::AV_COLS + 32 * pl, r);
           }
           tc_wait_st();
           tc_fence_before();
@@ -587,14 +598,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           for (int h = 0; h < GP; ++h) {
             // folded per-head constants (set-up): logit = nk (mse ak + bk) + gamma (qjl aq + bq)
             const float4 hc = *reinterpret_cast<const float4*>(s_head + h * 8);
-            const float mse = fmaf(0.00390625f, ds[3 * h + 2], fmaf(0.0625f, ds[3 * h + 1], ds[3 * h]));
-            const float qjl = fmaf(0.00390625f, ds[NHALF + 3 * h + 2], fmaf(0.0625f, ds[NHALF + 3 * h + 1], ds[NHALF + 3 * h]));
+            const float* dk = ds + 4 * h;
+            const float* dq = ds + NHALF + 4 * h;
+            const float mse = fmaf(0.000244140625f, dk[3], fmaf(0.00390625f, dk[2], fmaf(0.0625f, dk[1], dk[0])));
+            const float qjl = fmaf(0.000244140625f, dq[3], fmaf(0.00390625f, dq[2], fmaf(0.0625f, dq[1], dq[0])));
             const float l = fmaf(nk, fmaf(mse, hc.x, hc.y), gmv * fmaf(qjl, hc.z, hc.w));
             lg[h] = (valid && h < G) ? l : -INFINITY;
             if (a.logits && valid && h < G)
               a.logits[((size_t)b * a.q_heads + (size_t)kvh * G + h) * a.max_tokens + (size_t)(p_lo + p) * 128 + row] = l;
             if (lg[h] > m_run[h] + kTau) ovf = 1;
           }
+          float fh[GP];
+#pragma unroll
+          for (int h = 0; h < GP; ++h) fh[h] = 1.f;
+          bool rescale = false;
           if (t_vote_or(ovf)) {
 #pragma unroll
             for (int h = 0; h <= GP; ++h) {
@@ -607,7 +624,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
             float nvmax = 0.f;
             for (int w2 = 0; w2 < 4; ++w2) nvmax = fmaxf(nvmax, s_red[w2 * (GP + 1) + GP]);
             const float n_new = nvmax > n_ref ? 1.25f * nvmax : n_ref;
-            float fh[GP];
 #pragma unroll
             for (int h = 0; h < GP; ++h) {
               float mx = -INFINITY;
@@ -621,29 +637,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
               m_run[h] = m_new;
             }
             n_ref = n_new;
+            rescale = p > 0;
             t_sync();   // s_red reads done
-            if (p > 0) {
-              // D_v holds exactly the pages before p once the value MMAs of page p-1 are done;
-              // this warp rescales its lane quarter (32 coordinates) of every plane accumulator
-              wait_k(&v_fin[(g - 1) & 1], (g - 1) >> 1);
-              tc_fence_after();
+          }
+          if (p == 0) {
+            // a new segment: the flushed total starts at zero (the previous epilogue has read it)
+            uint32_t z[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll 1
-              for (int c0 = 0; c0 < PV * NVC; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(tl + C::TD_V + c0, r);
-                tc_wait_ld();
+            for (int c0 = 0; c0 < PV * NVC; c0 += 16) tmem_st16(tl + C::TD_ACC + c0, z);
+            tc_wait_st();
+          }
+          const bool flush = p > 0 && p % kFlush == 0;
+          if (rescale || flush) {
+            // D_v holds exactly the pages of this stretch before p once the value MMAs of page
+            // p-1 are done; this warp handles its lane quarter (32 coordinates): on a flush
+            // D_acc = (D_acc + D_v) f, otherwise D_acc *= f and D_v *= f (f = 1 without rescale)
+            wait_k(&v_fin[(g - 1) & 1], (g - 1) >> 1);
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < PV * NVC; c0 += 16) {
+              uint32_t rv[16], ra[16];
+              tmem_ld16(tl + C::TD_V + c0, rv);
+              tmem_ld16(tl + C::TD_ACC + c0, ra);
+              tc_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const int h = ((c0 + i) % NVC) >> 1;
-                  float fv = 0.f;
+              for (int i = 0; i < 16; ++i) {
+                const int h = ((c0 + i) % NVC) / NPW;
+                float fv = 1.f;
 #pragma unroll
-                  for (int hh = 0; hh < GP; ++hh) fv = hh == h ? fh[hh] : fv;
-                  r[i] = __float_as_uint(__uint_as_float(r[i]) * fv);
-                }
-                tmem_st16(tl + C::TD_V + c0, r);
+                for (int hh = 0; hh < GP; ++hh) fv = hh == h ? fh[hh] : fv;
+                const float dv = __uint_as_float(rv[i]), da = __uint_as_float(ra[i]);
+                ra[i] = __float_as_uint(flush ? (da + dv) * fv : da * fv);
+                rv[i] = __float_as_uint(dv * fv);
               }
-              tc_wait_st();
+              tmem_st16(tl + C::TD_ACC + c0, ra);
+              if (!flush) tmem_st16(tl + C::TD_V + c0, rv);
             }
+            tc_wait_st();
           }
           // softmax weights -> two e4m3 pieces per head; the byte for row n = 2h + piece
           const float xs = nvt * (n_ref > 0.f ? 1.f / n_ref : 0.f) * v_igamma * kSB;
@@ -733,17 +765,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
 #pragma unroll 1
         for (int pl = 0; pl < PV; ++pl) {
           const float al = a.alpha_v[pl];
+          float dv[NVC];
 #pragma unroll
           for (int c0 = 0; c0 < NVC; c0 += 16) {
-            uint32_t r[16];
+            uint32_t r[16], ra[16];
             tmem_ld16(tl + C::TD_V + pl * NVC + c0, r);
+            tmem_ld16(tl + C::TD_ACC + pl * NVC + c0, ra);
             tc_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              const int h = (c0 + i) >> 1;
-              if (h < GP) ov[h] += al * (__uint_as_float(r[i]) + 0.0625f * __uint_as_float(r[i + 1]));
-            }
+            for (int i = 0; i < 16; ++i) dv[c0 + i] = __uint_as_float(r[i]) + __uint_as_float(ra[i]);
           }
+#pragma unroll
+          for (int h = 0; h < GP; ++h) ov[h] += al * fmaf(0.0625f, dv[NPW * h + 1], dv[NPW * h]);
         }
       }
       const float nref = n_pages > 0 ? s_f[0] : 0.f;

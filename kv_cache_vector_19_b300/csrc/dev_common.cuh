@@ -138,9 +138,23 @@ __device__ __forceinline__ void split3(float v, uint32_t& hi, uint32_t& mid, uin
   lo = cvt_e4m3x2(0.f, 256.f * r2) & 0xFF;
 }
 
+// Four-piece split: v ~ p0 + p1 / 16 + p2 / 256 + p3 / 4096 (~2^-16 relative).
+__device__ __forceinline__ void split4(float v, uint32_t (&pc)[4]) {
+  float r = v;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    pc[k] = cvt_e4m3x2(0.f, r) & 0xFF;
+    r = 16.f * (r - e4m3x2_to_f2(pc[k]).x);
+  }
+}
+
 __device__ __forceinline__ float e4m3_val(uint32_t byte) { return e4m3x2_to_f2(byte).x; }
 __device__ __forceinline__ float split3_val(uint32_t hi, uint32_t mid, uint32_t lo) {
   return e4m3_val(hi) + 0.0625f * e4m3_val(mid) + 0.00390625f * e4m3_val(lo);
+}
+__device__ __forceinline__ float split4_val(const uint32_t (&pc)[4]) {
+  return e4m3_val(pc[0]) + 0.0625f * e4m3_val(pc[1]) + 0.00390625f * e4m3_val(pc[2]) +
+         0.000244140625f * e4m3_val(pc[3]);
 }
 
 
