@@ -235,6 +235,8 @@ extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, i
   if (!k || !v || !start_pos || !cache) return TQ_EINVAL;
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(cache, 256) || !aligned(start_pos, 4)) return TQ_EINVAL;
   DeviceGuard guard(ctx->device);
+  if (n_tokens <= tq::kFewTokens)
+    return tq::launch_quantize_few(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
   if (ctx->d == 128)
     return tq::launch_quantize_tc(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
   return launch_quantize_simt(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);

@@ -1,0 +1,143 @@
+// tq_quantize_kv for calls that write only a few tokens per sequence (decode-time appends):
+// one CTA per new (batch, kv head, token) vector pair, one thread per coordinate, fp32.
+//
+// [BLOG] "Технология TurboQuant и её применение с локальными LLM", section 1.2, for a
+// single vector: y = Pi x, Lloyd-Max code of y / ||x|| per coordinate (b-1 bits for the
+// key, b for the value); for the key the residual in the rotated frame, Pi r = y - n c[idx],
+// is projected by S' = S Pi^T (S r = S' Pi r) and only sign(S r) and ||r|| are kept.
+// The page-tile kernels process a whole 128-slot tile per page touched, so a one-token
+// append costs as much as a full page; here the two d x d products are matrix-vector
+// products against Pi^T and S'^T (L2-resident after the first CTA), and the slot is written
+// in place: its key-code, sign and norm words belong to it alone, and its bit of each value
+// word (a value word spans 32 slots) is set with an atomic.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "layout.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+template <int D>
+__device__ __forceinline__ float block_sum(float v, float* s_red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();   // s_red free
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < D / 32; ++w) t += s_red[w];
+  return t;
+}
+
+template <int D, int BITS>
+__global__ void __launch_bounds__(D) quantize_few_kernel(const __nv_bfloat16* __restrict__ k,
+                                                         const __nv_bfloat16* __restrict__ v, int kv_heads,
+                                                         int n_tokens, int max_tokens, int pages_per_seq,
+                                                         const int32_t* __restrict__ start_pos, uint8_t* cache,
+                                                         const float* __restrict__ pit, const float* __restrict__ spt,
+                                                         const float* __restrict__ ck, const float* __restrict__ tk,
+                                                         const float* __restrict__ cv, const float* __restrict__ tv,
+                                                         int* status) {
+  using PL = PageLayout<D, BITS>;
+  constexpr int M = D, BK = BITS - 1, BV = BITS, LK = 1 << BK, LV = 1 << BV;
+  __shared__ float s_xk[D], s_xv[D], s_r[D];
+  __shared__ float s_red[D / 32];
+  __shared__ uint32_t s_words[BK * PL::KW + PL::SW];   // the slot's key-code and sign words
+  const int j = threadIdx.x;
+  const int t = blockIdx.x, seq = blockIdx.y, b = seq / kv_heads;
+  const int start = start_pos[b];
+  if (start < 0 || start > max_tokens - n_tokens) {
+    if (j == 0 && t == 0) atomicOr(status, kFlagBounds);
+    return;
+  }
+  const int pos = start + t, page = pos >> 7, slot = pos & 127;
+  uint8_t* pg = cache + ((size_t)seq * pages_per_seq + page) * (size_t)PL::bytes;
+  const size_t row = ((size_t)seq * n_tokens + t) * D;
+  const float xk = __bfloat162float(k[row + j]), xv = __bfloat162float(v[row + j]);
+  s_xk[j] = xk;
+  s_xv[j] = xv;
+  if (j < BK * PL::KW + PL::SW) s_words[j] = 0u;
+  const float nk = sqrtf(block_sum<D>(xk * xk, s_red));   // also orders the s_xk / s_xv stores
+  const float nv = sqrtf(block_sum<D>(xv * xv, s_red));
+  // y_j = (Pi x)_j = sum_c Pi^T[c][j] x_c
+  float yk = 0.f, yv = 0.f;
+#pragma unroll 32
+  for (int c = 0; c < D; ++c) {
+    const float p = pit[(size_t)c * D + j];
+    yk = fmaf(p, s_xk[c], yk);
+    yv = fmaf(p, s_xv[c], yv);
+  }
+  // Lloyd-Max codes by boundary count (a value on a boundary takes the upper code)
+  const float ik = nk > 0.f ? 1.f / nk : 0.f, iv = nv > 0.f ? 1.f / nv : 0.f;
+  const float uk = yk * ik, uv = yv * iv;
+  int idx = 0, vidx = 0;
+#pragma unroll
+  for (int q = 0; q < LK - 1; ++q) idx += uk >= tk[q] ? 1 : 0;
+#pragma unroll
+  for (int q = 0; q < LV - 1; ++q) vidx += uv >= tv[q] ? 1 : 0;
+  const float r = yk - nk * ck[idx];   // residual in the rotated frame
+  s_r[j] = r;
+  const float gamma = sqrtf(block_sum<D>(r * r, s_red));
+  // z_i = (S' Pi r)_i = sum_c S'^T[c][i] (Pi r)_c; thread j computes z_j (m == d)
+  float z = 0.f;
+#pragma unroll 32
+  for (int c = 0; c < D; ++c) z = fmaf(spt[(size_t)c * M + j], s_r[c], z);
+  // the slot's words: coordinate j of each key-code plane and of the sign plane
+  int w, bit;
+  coord_pos<D>(j, w, bit);
+#pragma unroll
+  for (int q = 0; q < BK; ++q)
+    if ((idx >> q) & 1) atomicOr(&s_words[q * PL::KW + w], 1u << bit);
+  if (z >= 0.f) atomicOr(&s_words[BK * PL::KW + w], 1u << bit);
+  __syncthreads();
+  uint32_t* kc = reinterpret_cast<uint32_t*>(pg + PL::off_kcodes);
+  uint32_t* sg = reinterpret_cast<uint32_t*>(pg + PL::off_signs);
+  if (j < BK * PL::KW) kc[((j / PL::KW) * 128 + slot) * PL::KW + (j % PL::KW)] = s_words[j];
+  else if (j < BK * PL::KW + PL::SW) sg[slot * PL::SW + (j - BK * PL::KW)] = s_words[j];
+  if (j == 0) {
+    reinterpret_cast<float*>(pg + PL::off_nk)[slot] = nk;
+    reinterpret_cast<float*>(pg + PL::off_gamma)[slot] = gamma;
+    reinterpret_cast<float*>(pg + PL::off_nv)[slot] = nv;
+  }
+  // value code of coordinate j: one bit in each plane's word over this slot's group of 32
+  int vw, vb;
+  slot_pos(slot, vw, vb);
+  uint32_t* vc = reinterpret_cast<uint32_t*>(pg + PL::off_vcodes);
+#pragma unroll
+  for (int q = 0; q < BV; ++q) {
+    uint32_t* word = vc + ((size_t)q * D + j) * 4 + vw;
+    if ((vidx >> q) & 1) atomicOr(word, 1u << vb);
+    else atomicAnd(word, ~(1u << vb));
+  }
+}
+
+template <int D, int BITS>
+int launch_one(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
+               const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st) {
+  const dim3 grid((unsigned)n_tokens, (unsigned)(batch * kv_heads));
+  quantize_few_kernel<D, BITS><<<grid, D, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), kv_heads, n_tokens, max_tokens,
+      (max_tokens + 127) / 128, start_pos, static_cast<uint8_t*>(cache), c->d_pit, c->d_spt, c->d_ck, c->d_tk,
+      c->d_cv, c->d_tv, c->d_status);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
+}
+
+}  // namespace
+
+int launch_quantize_few(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
+                        const int32_t* start_pos, void* cache, int max_tokens, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+#define TQ_QF(DD, BB) \
+  if (c->d == DD && c->bits == BB) \
+    return launch_one<DD, BB>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st);
+  TQ_QF(64, 2) TQ_QF(64, 3) TQ_QF(64, 4) TQ_QF(64, 5) TQ_QF(128, 2) TQ_QF(128, 3) TQ_QF(128, 4) TQ_QF(128, 5)
+  TQ_QF(256, 2) TQ_QF(256, 3) TQ_QF(256, 4) TQ_QF(256, 5)
+#undef TQ_QF
+  return TQ_EUNSUPPORTED;
+}
+
+}  // namespace tq

@@ -140,7 +140,24 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
     // ---- stage K and V rows (slots outside [lo, hi) are zero); row norms on the way ----
     __syncthreads();   // previous item done with sK / sV
     if (*s_fail) break;   // uniform: a bounded wait gave up
-#pragma unroll 2
+    if (tid == 0) {
+      // the rows of this CTA's next item into L2 while this one is processed
+      const int nx = item + (int)gridDim.x;
+      if (nx < n_items) {
+        const int nip = nx % a.items_per_seq, nseq = nx / a.items_per_seq;
+        const int nstart = a.start_pos[nseq / a.kv_heads];
+        if (nstart >= 0 && nstart <= a.max_tokens - a.n_tokens) {
+          const int npage = nstart / 128 + nip;
+          const int nlo = max(nstart, npage * 128), nhi = min(nstart + a.n_tokens, npage * 128 + 128);
+          if (nlo < nhi) {
+            const size_t off = ((size_t)nseq * a.n_tokens + (size_t)(nlo - nstart)) * D;
+            prefetch_l2(a.k + off, (uint32_t)(nhi - nlo) * D * 2);
+            prefetch_l2(a.v + off, (uint32_t)(nhi - nlo) * D * 2);
+          }
+        }
+      }
+    }
+#pragma unroll 4
     for (int it = 0; it < 8; ++it) {
       const int c = tid + kThreads * it;   // 16-byte chunk: slot c / 16, chunk c % 16
       const int slot = c >> 4, kc = c & 15;

@@ -74,6 +74,10 @@ namespace tq {
 int prepare_quantize_tc(const tq_ctx* c);
 int launch_dequantize(const tq_ctx* c, const void* cache, int batch, int kv_heads, int max_tokens,
                       const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream);
+// Few tokens per sequence (appends): one CTA per new vector pair.
+constexpr int kFewTokens = 8;
+int launch_quantize_few(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
+                        const int32_t* start_pos, void* cache, int max_tokens, void* stream);
 int launch_quantize_tc(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
                        const int32_t* start_pos, void* cache, int max_tokens, void* stream);
 }  // namespace tq

@@ -138,6 +138,9 @@ def test_decode_long_sequences_each_kernel(path):
 
 
 def test_append_one_token_at_a_time_matches_bulk():
+    """Appends (one token per call: the few-token kernel) against one bulk call (the page-tile
+    kernel): the slots written before the appends are untouched, and the appended tokens meet
+    the same oracle bars as bulk-quantized ones (codes may differ only at a boundary)."""
     d, b, B, H, maxT = 128, 3, 2, 2, 300
     k, v = _inputs(B, H, 260, d, seed=5)
     bulk = P.Run(d, b, B, H, 8, maxT)
@@ -146,12 +149,37 @@ def test_append_one_token_at_a_time_matches_bulk():
     step.quantize(k[:, :, :250].contiguous(), v[:, :, :250].contiguous(), [0, 0])
     for t in range(250, 260):
         step.quantize(k[:, :, t:t + 1].contiguous(), v[:, :, t:t + 1].contiguous(), [t, t])
+    assert step.status() == tq.TQ_OK
     a, c = bulk.cache_np(), step.cache_np()
     for bb in range(B):
         for h in range(H):
             ta, tc = bulk.tokens(a, bb, h, 260), step.tokens(c, bb, h, 260)
             for key in ta:
-                assert np.array_equal(ta[key], tc[key]), key
+                assert np.array_equal(ta[key][:250], tc[key][:250]), key
+            sl = slice(250, 260)
+            got = {key: val[sl] for key, val in tc.items()}
+            res = P.compare_sequence(step, P.to64(k[bb, h, sl]), P.to64(v[bb, h, sl]), got)
+            P.assert_quantize_ok(res, rate=1e-3)
+            for key in ("nk", "nv", "gamma"):
+                assert np.allclose(tc[key][sl], ta[key][sl], rtol=1e-5, atol=1e-30), key
+
+
+def test_few_token_appends_every_format():
+    """The few-token kernel at every (d, b): appends of 1..8 tokens at unaligned slots."""
+    for d, b in ALL_DB:
+        run = P.Run(d, b, 1, 2, 2, 400)
+        k, v = _inputs(1, 2, 140, d, seed=30 + d + b)
+        run.quantize(k[:, :, :100].contiguous(), v[:, :, :100].contiguous(), [0])
+        t = 100
+        for n in (1, 3, 8, 5, 2, 1, 8, 8, 4):
+            run.quantize(k[:, :, t:t + n].contiguous(), v[:, :, t:t + n].contiguous(), [t])
+            t += n
+        assert run.status() == tq.TQ_OK
+        cache = run.cache_np()
+        for h in range(2):
+            tok = run.tokens(cache, 0, h, 140)
+            res = P.compare_sequence(run, P.to64(k[0, h]), P.to64(v[0, h]), tok)
+            P.assert_quantize_ok(res)
 
 
 def test_zero_vectors_and_tiny_sequences():
