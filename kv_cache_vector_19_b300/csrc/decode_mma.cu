@@ -27,10 +27,12 @@ namespace dmma {
 
 // Merges the partial records of one (query head, batch) and rotates back: out = Pi^T o~ / l.
 template <int D>
-__global__ void __launch_bounds__(D) combine_kernel(const float* __restrict__ part, const float* __restrict__ pi,
-                                                    float* __restrict__ out, int q_heads, int kv_heads, int group,
-                                                    int pages_per_seq, int chunk, int slots, int grid) {
+__global__ void __launch_bounds__(4 * D) combine_kernel(const float* __restrict__ part, const float* __restrict__ pi,
+                                                        float* __restrict__ out, int q_heads, int kv_heads, int group,
+                                                        int pages_per_seq, int chunk, int slots, int grid) {
+  constexpr int KQ = D / 4;
   __shared__ float s_o[D];
+  __shared__ float s_r[4][D];
   __shared__ float s_w[512];
   __shared__ float s_norm;
   const int hq = blockIdx.x, b = blockIdx.y;
@@ -39,9 +41,9 @@ __global__ void __launch_bounds__(D) combine_kernel(const float* __restrict__ pa
   const int first = (int)(((long)seq * pages_per_seq) / chunk);
   const int last = min(grid - 1, (int)(((long)(seq + 1) * pages_per_seq - 1) / chunk));
   const int n = last - first + 1;
-  const int j = threadIdx.x;
+  const int j = threadIdx.x % D, qp = threadIdx.x / D;   // 4 D threads: coordinate, quarter
   auto rec = [&](int s) { return part + (((size_t)seq * slots + s) * group + hh) * (2 + D); };
-  if (j == 0) {
+  if (threadIdx.x == 0) {
     float mx = -INFINITY;
     for (int s = 0; s < n; ++s) mx = fmaxf(mx, rec(s)[0]);
     float l = 0.f;
@@ -54,17 +56,26 @@ __global__ void __launch_bounds__(D) combine_kernel(const float* __restrict__ pa
     s_norm = l > 0.f ? 1.f / l : 0.f;
   }
   __syncthreads();
-  float acc = 0.f;
-  for (int s = 0; s < n; ++s) {
-    float w = s_w[s];
-    if (w != 0.f) acc = fmaf(w, rec(s)[2 + j], acc);
+  if (qp == 0) {
+    float acc = 0.f;
+    for (int s = 0; s < n; ++s) {
+      float w = s_w[s];
+      if (w != 0.f) acc = fmaf(w, rec(s)[2 + j], acc);
+    }
+    s_o[j] = acc * s_norm;
   }
-  s_o[j] = acc * s_norm;
   __syncthreads();
+  // out_j = sum_k Pi[k][j] o~[k], each quarter of k by one quarter of the threads with all of
+  // its loads in flight (Pi is usually out of L2 after the cache scan)
   float r = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < D; ++k) r = fmaf(pi[(size_t)k * D + j], s_o[k], r);   // Pi[k][j] o~[k]
-  out[row * D + j] = r;
+#pragma unroll
+  for (int kk = 0; kk < KQ; ++kk) {
+    const int k = qp * KQ + kk;
+    r = fmaf(pi[(size_t)k * D + j], s_o[k], r);
+  }
+  s_r[qp][j] = r;
+  __syncthreads();
+  if (qp == 0) out[row * D + j] = (s_r[0][j] + s_r[1][j]) + (s_r[2][j] + s_r[3][j]);
 }
 
 namespace {
@@ -126,7 +137,7 @@ int launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, in
     a.slots = pl.slots;
     a.total_pages = pl.total_pages;
     decode_mma_kernel<D, BITS, NGRP><<<pl.grid, kThreads, C::SMEM, st>>>(a);
-    combine_kernel<D><<<dim3(q_heads, batch), D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
+    combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
                                                           pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
   }
@@ -242,7 +253,7 @@ int tc_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
     a.slots = pl.slots;
     a.total_pages = pl.total_pages;
     dtc::decode_tc_kernel<BITS, GP><<<pl.grid, dtc::kThreads, C::SMEM, st>>>(a);
-    dmma::combine_kernel<D><<<dim3(q_heads, batch), D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
+    dmma::combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
                                                                 pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
   }

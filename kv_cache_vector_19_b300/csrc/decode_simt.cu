@@ -40,21 +40,32 @@ constexpr int kMaxG = 16;
 
 // q~ = Pi q and q_s = S q, one CTA of D threads per (query head, batch).
 template <int D>
-__global__ void __launch_bounds__(D) prologue_kernel(const float* __restrict__ q, const float* __restrict__ pit,
-                                                     const float* __restrict__ st, float* __restrict__ qr,
-                                                     float* __restrict__ qs, int q_heads) {
+__global__ void __launch_bounds__(4 * D) prologue_kernel(const float* __restrict__ q, const float* __restrict__ pit,
+                                                         const float* __restrict__ st, float* __restrict__ qr,
+                                                         float* __restrict__ qs, int q_heads) {
+  // 4 D threads: part p = tid / D sums k over its quarter of [0, D) with all of its matrix
+  // loads in flight at once (the matrices are usually out of L2 when a decode starts)
+  constexpr int KQ = D / 4;
   __shared__ float sq[D];
+  __shared__ float s_a[4][D], s_s[4][D];
   const size_t row = (size_t)blockIdx.y * q_heads + blockIdx.x;
-  const int j = threadIdx.x;
-  sq[j] = q[row * D + j];
+  const int j = threadIdx.x % D, part = threadIdx.x / D;
+  if (part == 0) sq[j] = q[row * D + j];
   __syncthreads();
   float a = 0.f, s = 0.f;
-  for (int k = 0; k < D; ++k) {
+#pragma unroll
+  for (int kk = 0; kk < KQ; ++kk) {
+    const int k = part * KQ + kk;
     a = fmaf(pit[(size_t)k * D + j], sq[k], a);   // Pi[j][k] q[k]
     s = fmaf(st[(size_t)k * D + j], sq[k], s);    // S[j][k] q[k]
   }
-  qr[row * D + j] = a;
-  qs[row * D + j] = s;
+  s_a[part][j] = a;
+  s_s[part][j] = s;
+  __syncthreads();
+  if (part == 0) {
+    qr[row * D + j] = (s_a[0][j] + s_a[1][j]) + (s_a[2][j] + s_a[3][j]);
+    qs[row * D + j] = (s_s[0][j] + s_s[1][j]) + (s_s[2][j] + s_s[3][j]);
+  }
 }
 
 struct DArgs {
@@ -286,7 +297,7 @@ int launch_d(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_hea
   float* qr = static_cast<float*>(ws);
   float* qs = qr + (size_t)batch * q_heads * D;
   float* part = qs + (size_t)batch * q_heads * D;
-  prologue_kernel<D><<<dim3(q_heads, batch), D, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
+  prologue_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
   DArgs a;
   a.qr = qr;
   a.qs = qs;
@@ -314,9 +325,9 @@ int launch_d(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_hea
 void launch_prologue(const tq_ctx* c, const float* q, int batch, int q_heads, float* qr, float* qs,
                      cudaStream_t st) {
   dim3 grid(q_heads, batch);
-  if (c->d == 64) prologue_kernel<64><<<grid, 64, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
-  if (c->d == 128) prologue_kernel<128><<<grid, 128, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
-  if (c->d == 256) prologue_kernel<256><<<grid, 256, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
+  if (c->d == 64) prologue_kernel<64><<<grid, 4 * 64, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
+  if (c->d == 128) prologue_kernel<128><<<grid, 4 * 128, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
+  if (c->d == 256) prologue_kernel<256><<<grid, 4 * 256, 0, st>>>(q, c->d_pit, c->d_st, qr, qs, q_heads);
 }
 
 }  // namespace tq

@@ -19,7 +19,8 @@
 namespace tq {
 namespace {
 
-template <int D>
+// Sum over the CTA's NT threads (every thread gets the total).
+template <int NT>
 __device__ __forceinline__ float block_sum(float v, float* s_red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -29,12 +30,12 @@ __device__ __forceinline__ float block_sum(float v, float* s_red) {
   __syncthreads();
   float t = 0.f;
 #pragma unroll
-  for (int w = 0; w < D / 32; ++w) t += s_red[w];
+  for (int w = 0; w < NT / 32; ++w) t += s_red[w];
   return t;
 }
 
 template <int D, int BITS>
-__global__ void __launch_bounds__(D) quantize_few_kernel(const __nv_bfloat16* __restrict__ k,
+__global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16* __restrict__ k,
                                                          const __nv_bfloat16* __restrict__ v, int kv_heads,
                                                          int n_tokens, int max_tokens, int pages_per_seq,
                                                          const int32_t* __restrict__ start_pos, uint8_t* cache,
@@ -44,33 +45,47 @@ __global__ void __launch_bounds__(D) quantize_few_kernel(const __nv_bfloat16* __
                                                          int* status) {
   using PL = PageLayout<D, BITS>;
   constexpr int M = D, BK = BITS - 1, BV = BITS, LK = 1 << BK, LV = 1 << BV;
+  constexpr int NT = 4 * D, KQ = D / 4;   // 4 D threads: coordinate j, quarter qp of each sum
   __shared__ float s_xk[D], s_xv[D], s_r[D];
-  __shared__ float s_red[D / 32];
+  __shared__ float s_pa[4][D], s_pb[4][D];   // partial sums of the quarters
+  __shared__ float s_red[NT / 32];
   __shared__ uint32_t s_words[BK * PL::KW + PL::SW];   // the slot's key-code and sign words
-  const int j = threadIdx.x;
+  const int j = threadIdx.x % D, qp = threadIdx.x / D;
   const int t = blockIdx.x, seq = blockIdx.y, b = seq / kv_heads;
   const int start = start_pos[b];
   if (start < 0 || start > max_tokens - n_tokens) {
-    if (j == 0 && t == 0) atomicOr(status, kFlagBounds);
+    if (threadIdx.x == 0 && t == 0) atomicOr(status, kFlagBounds);
     return;
   }
   const int pos = start + t, page = pos >> 7, slot = pos & 127;
   uint8_t* pg = cache + ((size_t)seq * pages_per_seq + page) * (size_t)PL::bytes;
   const size_t row = ((size_t)seq * n_tokens + t) * D;
-  const float xk = __bfloat162float(k[row + j]), xv = __bfloat162float(v[row + j]);
-  s_xk[j] = xk;
-  s_xv[j] = xv;
-  if (j < BK * PL::KW + PL::SW) s_words[j] = 0u;
-  const float nk = sqrtf(block_sum<D>(xk * xk, s_red));   // also orders the s_xk / s_xv stores
-  const float nv = sqrtf(block_sum<D>(xv * xv, s_red));
-  // y_j = (Pi x)_j = sum_c Pi^T[c][j] x_c
-  float yk = 0.f, yv = 0.f;
-#pragma unroll 32
-  for (int c = 0; c < D; ++c) {
-    const float p = pit[(size_t)c * D + j];
-    yk = fmaf(p, s_xk[c], yk);
-    yv = fmaf(p, s_xv[c], yv);
+  float xk = 0.f, xv = 0.f;
+  if (qp == 0) {
+    xk = __bfloat162float(k[row + j]);
+    xv = __bfloat162float(v[row + j]);
+    s_xk[j] = xk;
+    s_xv[j] = xv;
+    if (j < BK * PL::KW + PL::SW) s_words[j] = 0u;
   }
+  const float nk = sqrtf(block_sum<NT>(xk * xk, s_red));   // also orders the s_xk / s_xv stores
+  const float nv = sqrtf(block_sum<NT>(xv * xv, s_red));
+  // y_j = (Pi x)_j = sum_c Pi^T[c][j] x_c, one quarter of c per thread group, all loads in flight
+  {
+    float pa = 0.f, pb = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < KQ; ++cc) {
+      const int c = qp * KQ + cc;
+      const float p = pit[(size_t)c * D + j];
+      pa = fmaf(p, s_xk[c], pa);
+      pb = fmaf(p, s_xv[c], pb);
+    }
+    s_pa[qp][j] = pa;
+    s_pb[qp][j] = pb;
+  }
+  __syncthreads();
+  const float yk = (s_pa[0][j] + s_pa[1][j]) + (s_pa[2][j] + s_pa[3][j]);
+  const float yv = (s_pb[0][j] + s_pb[1][j]) + (s_pb[2][j] + s_pb[3][j]);
   // Lloyd-Max codes by boundary count (a value on a boundary takes the upper code)
   const float ik = nk > 0.f ? 1.f / nk : 0.f, iv = nv > 0.f ? 1.f / nv : 0.f;
   const float uk = yk * ik, uv = yv * iv;
@@ -80,12 +95,22 @@ __global__ void __launch_bounds__(D) quantize_few_kernel(const __nv_bfloat16* __
 #pragma unroll
   for (int q = 0; q < LV - 1; ++q) vidx += uv >= tv[q] ? 1 : 0;
   const float r = yk - nk * ck[idx];   // residual in the rotated frame
-  s_r[j] = r;
-  const float gamma = sqrtf(block_sum<D>(r * r, s_red));
-  // z_i = (S' Pi r)_i = sum_c S'^T[c][i] (Pi r)_c; thread j computes z_j (m == d)
-  float z = 0.f;
-#pragma unroll 32
-  for (int c = 0; c < D; ++c) z = fmaf(spt[(size_t)c * M + j], s_r[c], z);
+  if (qp == 0) s_r[j] = r;
+  const float gamma = sqrtf(block_sum<NT>(qp == 0 ? r * r : 0.f, s_red));
+  // z_i = (S' Pi r)_i = sum_c S'^T[c][i] (Pi r)_c; thread (j, qp) sums quarter qp for z_j (m == d)
+  {
+    float pz = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < KQ; ++cc) {
+      const int c = qp * KQ + cc;
+      pz = fmaf(spt[(size_t)c * M + j], s_r[c], pz);
+    }
+    __syncthreads();   // s_pa reads (y) done
+    s_pa[qp][j] = pz;
+  }
+  __syncthreads();
+  const float z = (s_pa[0][j] + s_pa[1][j]) + (s_pa[2][j] + s_pa[3][j]);
+  if (qp != 0) return;   // the rest is per coordinate
   // the slot's words: coordinate j of each key-code plane and of the sign plane
   int w, bit;
   coord_pos<D>(j, w, bit);
@@ -93,7 +118,7 @@ __global__ void __launch_bounds__(D) quantize_few_kernel(const __nv_bfloat16* __
   for (int q = 0; q < BK; ++q)
     if ((idx >> q) & 1) atomicOr(&s_words[q * PL::KW + w], 1u << bit);
   if (z >= 0.f) atomicOr(&s_words[BK * PL::KW + w], 1u << bit);
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"r"(D) : "memory");   // the D remaining threads (warps 0 .. D/32-1)
   uint32_t* kc = reinterpret_cast<uint32_t*>(pg + PL::off_kcodes);
   uint32_t* sg = reinterpret_cast<uint32_t*>(pg + PL::off_signs);
   if (j < BK * PL::KW) kc[((j / PL::KW) * 128 + slot) * PL::KW + (j % PL::KW)] = s_words[j];
@@ -119,7 +144,7 @@ template <int D, int BITS>
 int launch_one(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
                const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st) {
   const dim3 grid((unsigned)n_tokens, (unsigned)(batch * kv_heads));
-  quantize_few_kernel<D, BITS><<<grid, D, 0, st>>>(
+  quantize_few_kernel<D, BITS><<<grid, 4 * D, 0, st>>>(
       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), kv_heads, n_tokens, max_tokens,
       (max_tokens + 127) / 128, start_pos, static_cast<uint8_t*>(cache), c->d_pit, c->d_spt, c->d_ck, c->d_tk,
       c->d_cv, c->d_tv, c->d_status);
