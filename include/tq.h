@@ -209,6 +209,12 @@ int tq_attn_decode_noalloc(const tq_ctx* ctx, const float* q, int batch, int q_h
 int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch, int kv_heads, int max_tokens,
                      const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream);
 
+/* Self-test of the device-side failure path: launches one thread that waits, with the same
+ * bounded wait every kernel uses, on an mbarrier nothing arrives at.  The wait gives up after
+ * its limit (2 s), sets the sticky timeout flag and the kernel returns; a following
+ * tq_get_device_status reports TQ_ETIMEOUT.  Nothing faults or hangs. */
+int tq_selftest_bounded_wait(const tq_ctx* ctx, void* stream);
+
 /* Synchronises `stream`, then returns and clears the sticky device status: TQ_OK,
  * TQ_EBOUNDS or TQ_ETIMEOUT. */
 int tq_get_device_status(const tq_ctx* ctx, void* stream);

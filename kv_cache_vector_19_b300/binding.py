@@ -53,6 +53,7 @@ _SIGS = {
                                 _c_size, _vp]),
     "tq_attn_decode_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp]),
     "tq_dequantize_kv": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp]),
+    "tq_selftest_bounded_wait": (_c_int, [_vp, _vp]),
     "tq_get_device_status": (_c_int, [_vp, _vp]),
     "tq_status_string": (ctypes.c_char_p, [_c_int]),
 }

@@ -343,6 +343,12 @@ extern "C" int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch,
   return tq::launch_dequantize(ctx, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, stream);
 }
 
+extern "C" int tq_selftest_bounded_wait(const tq_ctx* ctx, void* stream) {
+  if (!ctx) return TQ_EINVAL;
+  DeviceGuard guard(ctx->device);
+  return tq::launch_selftest_wait(ctx, stream);
+}
+
 extern "C" int tq_get_device_status(const tq_ctx* ctx, void* stream) {
   if (!ctx) return TQ_EINVAL;
   DeviceGuard guard(ctx->device);

@@ -72,6 +72,7 @@ struct tq_ctx {
 int prepare_quantize_simt(const tq_ctx* ctx);
 namespace tq {
 int prepare_quantize_tc(const tq_ctx* c);
+int launch_selftest_wait(const tq_ctx* c, void* stream);
 int launch_dequantize(const tq_ctx* c, const void* cache, int batch, int kv_heads, int max_tokens,
                       const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream);
 // Few tokens per sequence (appends): one CTA per new vector pair.

@@ -270,3 +270,24 @@ def test_tiny_workload_full():
         assert np.max(np.abs(lg[0, hq] - l_pages)) < P.LOGIT_ATOL
         o_e2e, _ = P.oracle_end_to_end(run, qrow, res["oracle_k"], res["oracle_v"])
         assert P.rel_l2(out[0, hq], o_e2e) < P.OUT_REL_L2
+
+
+def test_bounded_wait_times_out_and_reports():
+    """A device-side wait that can never complete gives up after its limit: the kernel
+    returns, the sticky status reads TQ_ETIMEOUT once, and the context stays usable."""
+    import time
+    run = P.Run(128, 3, 1, 1, 4, 256)
+    t0 = time.time()
+    assert tq.lib().tq_selftest_bounded_wait(run.ctx.handle, binding_stream()) == tq.TQ_OK
+    assert run.status() == tq.TQ_ETIMEOUT
+    assert time.time() - t0 < 30
+    assert run.status() == tq.TQ_OK            # the flag is cleared by the read
+    k, v = _inputs(1, 1, 20, 128, seed=1)
+    run.quantize(k, v, [0])                    # the context still works
+    out, _ = run.decode(torch.randn(1, 4, 128), [20])
+    assert run.status() == tq.TQ_OK and torch.isfinite(out).all()
+
+
+def binding_stream():
+    from kv_cache_vector_19_b300 import binding
+    return binding._stream_handle(None)
