@@ -252,7 +252,7 @@ int tc_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
     a.chunk = pl.chunk;
     a.slots = pl.slots;
     a.total_pages = pl.total_pages;
-    dtc::decode_tc_kernel<BITS, GP><<<pl.grid, dtc::kThreads, C::SMEM, st>>>(a);
+    dtc::decode_tc_kernel<BITS, GP><<<pl.grid, C::THREADS, C::SMEM, st>>>(a);
     dmma::combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
                                                                 pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;

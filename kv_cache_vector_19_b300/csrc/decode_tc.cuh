@@ -44,8 +44,7 @@ namespace dtc {
 using namespace dev;
 using dmma::Params;
 
-constexpr int kWarps = 16;            // 4 token, 4 key-plane, 4 value-plane, 2 issuers, 2 waiters
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarpsBase = 16;        // 4 token, 4 key-plane, 4 value-plane, 2 issuers, 2 waiters
 constexpr int kWarpS = 12;            // issues the score MMAs
 constexpr int kWarpM = 13;            // issues the value MMAs
 constexpr int kWarpWS = 14;           // waits for the score operands, hands them to kWarpS
@@ -68,6 +67,12 @@ struct Cfg {
   using PL = PageLayout<128, BITS>;
   static constexpr int BK = BITS - 1, BV = BITS;
   static constexpr int PK = 1 << (BK - 1), PV = 1 << (BV - 1), NS = PK + 1;
+  // token warps: TS sets of four (one per TMEM lane quarter); set s handles HPT query heads
+  // from head s * HPT (a second set, warps 16-19, when a KV head carries 8 or more)
+  static constexpr int TS = GP >= 8 ? 2 : 1;
+  static constexpr int HPT = GP / TS;
+  static constexpr int WARPS = kWarpsBase + 4 * (TS - 1);
+  static constexpr int THREADS = 32 * WARPS;
   static constexpr int NQP = 4;                          // e4m3 pieces per query coordinate
   static constexpr int NHALF = rnd(NQP * GP, 8);       // score columns: [key term | sign term]
   static constexpr int NSC = rnd(2 * NHALF, 16);
@@ -97,8 +102,8 @@ struct Cfg {
   static constexpr int OFF_BV = OFF_BS + BS_BYTES;
   static constexpr int OFF_Q = OFF_BV + 2 * BV_BYTES;            // [GP][2][128] f32
   static constexpr int OFF_HEAD = OFF_Q + GP * 2 * 128 * 4;      // [GP][8] f32
-  static constexpr int OFF_RED = OFF_HEAD + GP * 8 * 4;          // [4 warps][GP + 1][3] f32
-  static constexpr int OFF_F = OFF_RED + 4 * (GP + 1) * 3 * 4;   // n_ref of the segment
+  static constexpr int OFF_RED = OFF_HEAD + GP * 8 * 4;          // [4 TS token warps][HPT + 1][3] f32
+  static constexpr int OFF_F = OFF_RED + 4 * TS * (HPT + 1) * 3 * 4;   // n_ref of the segment
   static constexpr int OFF_MBAR = rnd(OFF_F + 16, 8);
   // full[8], empty[8], as_ready[2], as_free[2], s_fin[2], ds_free[2], av_ready[2], v_fin[2],
   // bv_ready[2], teardown[2]
@@ -111,17 +116,19 @@ struct Cfg {
   static constexpr bool SUPPORTED = TCOLS <= 512 && SMEM <= kSmemMax && NBUF >= 4;
 };
 
-// OR-vote / barrier among the four token warps (named barrier 1).
+// OR-vote / barrier among the token warps (named barrier 1, NT = 128 or 256 threads).
+template <int NT>
 __device__ __forceinline__ int t_vote_or(int pred) {
   int r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.s32 q, %1, 0;\n barrier.cta.red.or.pred p, 1, 128, q;\n selp.s32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p, q;\n setp.ne.s32 q, %1, 0;\n barrier.cta.red.or.pred p, 1, %2, q;\n selp.s32 %0, 1, 0, p;\n}\n"
       : "=r"(r)
-      : "r"(pred)
+      : "r"(pred), "n"(NT)
       : "memory");
   return r;
 }
-__device__ __forceinline__ void t_sync() { asm volatile("barrier.cta.sync 1, 128;" ::: "memory"); }
+template <int NT>
+__device__ __forceinline__ void t_sync() { asm volatile("barrier.cta.sync 1, %0;" ::"n"(NT) : "memory"); }
 
 // The two MMA-issuing warps never wait on an mbarrier: on B300 a shared-memory access by a
 // thread with MMAs in flight (an mbarrier wait included) stalls it for hundreds of cycles,
@@ -186,11 +193,12 @@ __device__ __forceinline__ void expand_words(const uint32_t (&x)[4], uint32_t (&
 }
 
 template <int BITS, int GP>
-__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
+__global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Params a) {
   using C = Cfg<BITS, GP>;
   using PL = typename C::PL;
   constexpr int D = 128, NS = C::NS, PK = C::PK, PV = C::PV, BK = C::BK, BV = C::BV, NBUF = C::NBUF;
   constexpr int NSC = C::NSC, NVC = C::NVC, NHALF = C::NHALF, DSB = C::DSB, NPW = C::NPW, AVB = C::AVB;
+  constexpr int TS = C::TS, HPT = C::HPT, kThreads = C::THREADS, kWarps = C::WARPS, TNT = 128 * TS;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint8_t* s_pages = smem + C::OFF_PAGES;
   uint8_t* s_as = smem + C::OFF_AS;
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
   // per page of that parity, and every waiter has waited the previous completion: a parity
   // wait can therefore never mistake an older phase for a newer one.
   uint64_t* s_full = mb;            // [8]  page in ring slot landed (+ tx bytes)
-  uint64_t* s_empty = mb + 8;       // [8]  page read by every consumer warp (12)
+  uint64_t* s_empty = mb + 8;       // [8]  page read by every consumer warp (8 + 4 TS)
   uint64_t* as_ready = mb + 16;     // [2]  key planes of the page stored in A_s (4 warps)
   uint64_t* as_free = mb + 18;      // [2]  score MMAs reading that A_s buffer done (commit)
   uint64_t* s_fin = mb + 20;        // [2]  score MMAs into that D_s buffer done (commit)
@@ -231,16 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
   if (tid == 0) {
     for (int i = 0; i < 8; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 12);
+      mbar_init(&s_empty[i], 8 + 4 * TS);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&as_ready[i], 4);
       mbar_init(&as_free[i], 1);
       mbar_init(&s_fin[i], 1);
-      mbar_init(&ds_free[i], 4);
+      mbar_init(&ds_free[i], 4 * TS);
       mbar_init(&av_ready[i], 4);
       mbar_init(&v_fin[i], 1);
-      mbar_init(&bv_ready[i], 4);
+      mbar_init(&bv_ready[i], 4 * TS);
       mbar_init(&td_bar[i], 1);
     }
     *s_fail = 0;
@@ -558,7 +566,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&av_ready[x]);
         }
-      } else if (warp < 4) {
+      } else if (warp < 4 || warp >= kWarpsBase) {
+      if constexpr (TS == 1) {
+        // one set of token warps (heads per KV head <= 4)
         // ============ token warps (lane = token): logits, lazy softmax, weight operand ============
         float m_run[GP], l_part[GP], c_part[GP], g_part[GP];
 #pragma unroll
@@ -612,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
 #pragma unroll
           for (int h = 0; h < GP; ++h) fh[h] = 1.f;
           bool rescale = false;
-          if (t_vote_or(ovf)) {
+          if (t_vote_or<128>(ovf)) {
 #pragma unroll
             for (int h = 0; h <= GP; ++h) {
               float mx = h < GP ? lg[h] : nvt;
@@ -620,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
               for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
               if (lane == 0) s_red[warp * (GP + 1) + h] = mx;
             }
-            t_sync();
+            t_sync<128>();
             float nvmax = 0.f;
             for (int w2 = 0; w2 < 4; ++w2) nvmax = fmaxf(nvmax, s_red[w2 * (GP + 1) + GP]);
             const float n_new = nvmax > n_ref ? 1.25f * nvmax : n_ref;
@@ -638,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
             }
             n_ref = n_new;
             rescale = p > 0;
-            t_sync();   // s_red reads done
+            t_sync<128>();   // s_red reads done
           }
           if (p == 0) {
             // a new segment: the flushed total starts at zero (the previous epilogue has read it)
@@ -735,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
         }
         if (tid == 0) s_f[0] = n_ref;
         // partial record head part (m, l)
-        t_sync();
+        t_sync<128>();
         if (tid < GP && tid < G) {
           float l_tot = 0.f;
           for (int w2 = 0; w2 < 4; ++w2) l_tot += s_red[(w2 * (GP + 1) + tid) * 3];
@@ -743,6 +753,209 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
           rh[0] = m_run[tid];
           rh[1] = l_tot;
         }
+      } else {
+        // ============ token warps (lane = token): logits, lazy softmax, weight operand ============
+        // set ts of TS handles heads h0 .. h0 + HPT - 1; it owns their D_s columns, their D_v
+        // and D_acc columns and their B_v rows, so the sets never write the same word
+        const int twarp = warp < 4 ? warp : 4 + (warp - kWarpsBase);   // 0 .. 4 TS - 1
+        const int ts = TS == 1 ? 0 : twarp >> 2, h0 = ts * HPT;   // compile-time 0 with one set
+        float m_run[HPT], l_part[HPT], c_part[HPT], g_part[HPT];
+#pragma unroll
+        for (int h = 0; h < HPT; ++h) {
+          m_run[h] = -INFINITY;
+          l_part[h] = c_part[h] = g_part[h] = 0.f;
+        }
+        float n_ref = 0.f;
+        for (int p = 0; p < n_pages; ++p) {
+          const uint32_t g = pg_base + p, x = g & 1, db = DSB == 2 ? x : 0;
+          const uint8_t* pgp = pg_ptr(p);
+          wait_k(&s_full[ring_slot(p)], ring_use(p));
+          const int nvalid = min(128, seq_len - (p_lo + p) * 128);
+          const bool valid = row < nvalid;
+          const float nk = valid ? reinterpret_cast<const float*>(pgp + PL::off_nk)[row] : 0.f;
+          const float gmv = valid ? reinterpret_cast<const float*>(pgp + PL::off_gamma)[row] : 0.f;
+          const float nvt = valid ? reinterpret_cast<const float*>(pgp + PL::off_nv)[row] : 0.f;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
+          wait_k(&s_fin[x], g >> 1);        // every score MMA of page p is done
+          tc_fence_after();
+          float dsk[4 * HPT], dsq[4 * HPT];   // this set's key-term and sign-term columns
+#pragma unroll
+          for (int c0 = 0; c0 < 4 * HPT; c0 += 16) {
+            uint32_t r[16], rq[16];
+            tmem_ld16(tl + C::TD_S + db * C::DS_COLS + 4 * h0 + c0, r);
+            tmem_ld16(tl + C::TD_S + db * C::DS_COLS + NHALF + 4 * h0 + c0, rq);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              dsk[c0 + i] = __uint_as_float(r[i]);
+              dsq[c0 + i] = __uint_as_float(rq[i]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ds_free[x]);
+          float lg[HPT];
+          int ovf = nvt > n_ref;
+#pragma unroll
+          for (int h = 0; h < HPT; ++h) {
+            const int hg = h0 + h;
+            // folded per-head constants (set-up): logit = nk (mse ak + bk) + gamma (qjl aq + bq)
+            const float4 hc = *reinterpret_cast<const float4*>(s_head + hg * 8);
+            const float* dk = dsk + 4 * h;
+            const float* dq = dsq + 4 * h;
+            const float mse = fmaf(0.000244140625f, dk[3], fmaf(0.00390625f, dk[2], fmaf(0.0625f, dk[1], dk[0])));
+            const float qjl = fmaf(0.000244140625f, dq[3], fmaf(0.00390625f, dq[2], fmaf(0.0625f, dq[1], dq[0])));
+            const float l = fmaf(nk, fmaf(mse, hc.x, hc.y), gmv * fmaf(qjl, hc.z, hc.w));
+            lg[h] = (valid && hg < G) ? l : -INFINITY;
+            if (a.logits && valid && hg < G)
+              a.logits[((size_t)b * a.q_heads + (size_t)kvh * G + hg) * a.max_tokens + (size_t)(p_lo + p) * 128 + row] = l;
+            if (lg[h] > m_run[h] + kTau) ovf = 1;
+          }
+          float fh[HPT];
+#pragma unroll
+          for (int h = 0; h < HPT; ++h) fh[h] = 1.f;
+          bool rescale = false;
+          if (t_vote_or<TNT>(ovf)) {
+#pragma unroll
+            for (int h = 0; h <= HPT; ++h) {
+              float mx = h < HPT ? lg[h] : nvt;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+              if (lane == 0) s_red[twarp * (HPT + 1) + h] = mx;
+            }
+            t_sync<TNT>();
+            float nvmax = 0.f;
+            for (int w2 = 0; w2 < 4 * TS; ++w2) nvmax = fmaxf(nvmax, s_red[w2 * (HPT + 1) + HPT]);
+            const float n_new = nvmax > n_ref ? 1.25f * nvmax : n_ref;
+#pragma unroll
+            for (int h = 0; h < HPT; ++h) {
+              float mx = -INFINITY;
+              for (int w2 = 4 * ts; w2 < 4 * ts + 4; ++w2) mx = fmaxf(mx, s_red[w2 * (HPT + 1) + h]);
+              const float m_new = fmaxf(m_run[h], mx);
+              const float alpha = (m_run[h] == -INFINITY) ? 0.f : __expf(m_run[h] - m_new);
+              fh[h] = (n_ref > 0.f) ? alpha * (n_ref / n_new) : 0.f;
+              l_part[h] *= alpha;
+              c_part[h] *= fh[h];
+              g_part[h] *= fh[h];
+              m_run[h] = m_new;
+            }
+            n_ref = n_new;
+            rescale = p > 0;
+            t_sync<TNT>();   // s_red reads done
+          }
+          // this set's columns of each plane accumulator: pl NVC + NPW h0 .. + NPW HPT
+          if (p == 0) {
+            // a new segment: the flushed total starts at zero (the previous epilogue has read it)
+            uint32_t z[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) z[i] = 0u;
+#pragma unroll 1
+            for (int pl = 0; pl < PV; ++pl)
+              for (int co = 0; co < NPW * HPT; co += 8) tmem_st8(tl + C::TD_ACC + pl * NVC + NPW * h0 + co, z);
+            tc_wait_st();
+          }
+          const bool flush = p > 0 && p % kFlush == 0;
+          if (rescale || flush) {
+            // D_v holds exactly the pages of this stretch before p once the value MMAs of page
+            // p-1 are done; this warp handles its lane quarter (32 coordinates): on a flush
+            // D_acc = (D_acc + D_v) f, otherwise D_acc *= f and D_v *= f (f = 1 without rescale)
+            wait_k(&v_fin[(g - 1) & 1], (g - 1) >> 1);
+            tc_fence_after();
+#pragma unroll 1
+            for (int pl = 0; pl < PV; ++pl) {
+#pragma unroll
+              for (int co = 0; co < NPW * HPT; co += 8) {
+                const uint32_t col = pl * NVC + NPW * h0 + co;
+                uint32_t rv[8], ra[8];
+                tmem_ld8(tl + C::TD_V + col, rv);
+                tmem_ld8(tl + C::TD_ACC + col, ra);
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float fv = fh[(co + i) / NPW];
+                  const float dv = __uint_as_float(rv[i]), da = __uint_as_float(ra[i]);
+                  ra[i] = __float_as_uint(flush ? (da + dv) * fv : da * fv);
+                  rv[i] = __float_as_uint(dv * fv);
+                }
+                tmem_st8(tl + C::TD_ACC + col, ra);
+                if (!flush) tmem_st8(tl + C::TD_V + col, rv);
+              }
+            }
+            tc_wait_st();
+          }
+          // softmax weights -> two e4m3 pieces per head; the byte for row n = 2 hg + piece
+          const float xs = nvt * (n_ref > 0.f ? 1.f / n_ref : 0.f) * v_igamma * kSB;
+          uint32_t wb[HPT / 2];
+          // two heads per conversion: word h/2 holds rows 2h..2h+3 = [hi(h), lo(h), hi(h+1), lo(h+1)]
+#pragma unroll
+          for (int h = 0; h < HPT; h += 2) {
+            const float p0 = lg[h] == -INFINITY ? 0.f : __expf(lg[h] - m_run[h]);
+            const float p1 = lg[h + 1] == -INFINITY ? 0.f : __expf(lg[h + 1] - m_run[h + 1]);
+            l_part[h] += p0;
+            l_part[h + 1] += p1;
+            const float x0 = p0 * xs, x1 = p1 * xs;
+            const uint32_t hi2 = cvt_e4m3x2(x1, x0);
+            const float2 hf = e4m3x2_to_f2(hi2);
+            const uint32_t lo2 = cvt_e4m3x2(16.f * (x1 - hf.y), 16.f * (x0 - hf.x));
+            const float2 lf = e4m3x2_to_f2(lo2);
+            const float b0 = fmaf(0.0625f, lf.x, hf.x), b1 = fmaf(0.0625f, lf.y, hf.y);
+            c_part[h] = fmaf(v_beta, b0, c_part[h]);
+            c_part[h + 1] = fmaf(v_beta, b1, c_part[h + 1]);
+            g_part[h] = fmaf(v_gamma, b0, g_part[h]);
+            g_part[h + 1] = fmaf(v_gamma, b1, g_part[h + 1]);
+            wb[h >> 1] = __byte_perm(hi2, lo2, 0x5140);
+          }
+          // B_v buffer of page p: its previous user, the value MMA of page p-2, must be done
+          if (p >= 2) wait_k(&v_fin[g & 1], (g >> 1) - 1);
+          uint8_t* bvb = s_bv + (g & 1) * C::BV_BYTES;
+          const int e = lane & 3, base = lane & ~3;
+          const int k0 = 32 * ((row >> 2) & 3) + 4 * (row >> 4);   // K byte of token 4i
+          // this set's words (rows 4 w .. 4 w + 3); the last set also writes the zero padding rows
+          constexpr int NW_PAD = NVC / 4 - GP / 2;
+#pragma unroll
+          for (int r4 = 0; r4 < HPT / 2 + NW_PAD; ++r4) {
+            if (r4 >= HPT / 2 && ts != TS - 1) break;
+            const uint32_t wv = r4 < HPT / 2 ? wb[r4 < HPT / 2 ? r4 : 0] : 0u;
+            const uint32_t w0 = __shfl_sync(0xffffffffu, wv, base + 0);
+            const uint32_t w1 = __shfl_sync(0xffffffffu, wv, base + 1);
+            const uint32_t w2 = __shfl_sync(0xffffffffu, wv, base + 2);
+            const uint32_t w3 = __shfl_sync(0xffffffffu, wv, base + 3);
+            const uint32_t sel = (uint32_t)e | ((uint32_t)(e + 4) << 4);
+            const uint32_t t01 = __byte_perm(w0, w1, sel), t23 = __byte_perm(w2, w3, sel);
+            const int word = r4 < HPT / 2 ? h0 / 2 + r4 : GP / 2 + (r4 - HPT / 2);
+            *reinterpret_cast<uint32_t*>(bvb + canon_off(4 * word + e, k0, 128)) = __byte_perm(t01, t23, 0x5410);
+          }
+          fence_proxy_async();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bv_ready[g & 1]);
+        }
+        // per-head sums of this segment
+#pragma unroll
+        for (int h = 0; h < HPT; ++h) {
+          float v3[3] = {l_part[h], c_part[h], g_part[h]};
+#pragma unroll
+          for (int c = 0; c < 3; ++c) {
+            float v = v3[c];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) s_red[(twarp * (HPT + 1) + h) * 3 + c] = v;
+          }
+        }
+        if (tid == 0) s_f[0] = n_ref;
+        // partial record head part (m, l): lane h of the set's first warp for head h0 + h
+        t_sync<TNT>();
+        if ((twarp & 3) == 0 && lane < HPT && h0 + lane < G) {
+          float l_tot = 0.f, mv = 0.f;
+          for (int w2 = 4 * ts; w2 < 4 * ts + 4; ++w2) l_tot += s_red[(w2 * (HPT + 1) + lane) * 3];
+#pragma unroll
+          for (int h = 0; h < HPT; ++h) mv = h == lane ? m_run[h] : mv;
+          float* rh = rec + (size_t)(h0 + lane) * (2 + D);
+          rh[0] = mv;
+          rh[1] = l_tot;
+        }
+      }
       }
     }
     if (n_pages == 0 && warp == 0 && tid < GP && tid < G) {
@@ -785,11 +998,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(Params a) {
       for (int h = 0; h < GP; ++h) {
         if (h >= G) continue;
         float c_tot = 0.f, g_tot = 0.f;
-        if (n_pages > 0)
-          for (int w2 = 0; w2 < 4; ++w2) {
-            c_tot += s_red[(w2 * (GP + 1) + h) * 3 + 1];
-            g_tot += s_red[(w2 * (GP + 1) + h) * 3 + 2];
+        if (n_pages > 0) {
+          const int hs = h / HPT, hl = h % HPT;   // the token-warp set that summed head h
+          for (int w2 = 4 * hs; w2 < 4 * hs + 4; ++w2) {
+            c_tot += s_red[(w2 * (HPT + 1) + hl) * 3 + 1];
+            g_tot += s_red[(w2 * (HPT + 1) + hl) * 3 + 2];
           }
+        }
         const float o = scale * (2.f * (ov[h] - a.asum_v * c_tot) - a.asum_v * g_tot);
         rec[(size_t)h * (2 + D) + 2 + row] = n_pages > 0 ? o : 0.f;
       }
