@@ -6,19 +6,21 @@
 // position scales folded into the other operand.  What changes is where the MMAs run:
 //   A_s (smem, K-major, x2)       key planes and the sign plane of one page (row = token),
 //                                 NS x 128 bytes per row
-//   B_s (smem, K-major)           query pieces: 3 e4m3 pieces per head for the key term and
-//                                 3 for the sign term (columns), one row block per plane
+//   B_s (smem, K-major)           query pieces: 4 e4m3 pieces per head for the key term and
+//                                 4 for the sign term (columns), one row block per plane
 //   D_s (TMEM, lane = token, x2)  score partial sums, read back by the token warps
 //   A_v (TMEM, lane = coordinate, x2) value planes of one page, PV x 128 bytes
 //   B_v (smem, K-major, x2)       softmax weights of the page, 2 e4m3 pieces per head
-//   D_v (TMEM, lane = coordinate) one accumulator per value plane, kept across pages
+//   D_v (TMEM, lane = coordinate) one accumulator per value plane, restarted every kFlush pages
+//   D_acc (TMEM)                  fp32 running total of the flushed D_v stretches
 // Every per-page operand is double-buffered, so each producer / consumer pair has two pages
 // in flight and hands over once per page: a hand-off costs a few hundred cycles on B300, and
 // chains with one page in flight were what bounded earlier versions of this kernel.
 //
-// Warp roles, 16 warps, handing work over through mbarriers (no CTA barrier per page):
-//   warps 0-3   token warps (TMEM lane = token): read D_s, form logits, run the lazy online
-//               softmax, write B_v and, when the running maximum moves, rescale D_v
+// Warp roles, 20 warps, handing work over through mbarriers (no CTA barrier per page):
+//   warps 0-3, 16-19  token warps (TMEM lane = token), two sets each owning half of the query
+//               heads: read D_s, form logits, run the lazy online softmax, write B_v and, when
+//               the running maximum moves or a stretch ends, rescale or flush D_v
 //   warps 4-7   key-plane warps (row = token): key XOR planes and the sign plane -> A_s
 //   warps 8-11  value-plane warps (lane = coordinate): value XOR planes -> A_v; epilogue
 //   warp 12     issues the score MMAs (12 per page at b = 3), warp 13 the value MMAs (16)
@@ -44,7 +46,8 @@ namespace dtc {
 using namespace dev;
 using dmma::Params;
 
-constexpr int kWarpsBase = 16;        // 4 token, 4 key-plane, 4 value-plane, 2 issuers, 2 waiters
+constexpr int kWarpsBase = 16;        // 4 token, 4 key-plane, 4 value-plane, 2 issuers, 2 waiters;
+                                      // the second token-warp set follows
 constexpr int kWarpS = 12;            // issues the score MMAs
 constexpr int kWarpM = 13;            // issues the value MMAs
 constexpr int kWarpWS = 14;           // waits for the score operands, hands them to kWarpS
@@ -67,9 +70,11 @@ struct Cfg {
   using PL = PageLayout<128, BITS>;
   static constexpr int BK = BITS - 1, BV = BITS;
   static constexpr int PK = 1 << (BK - 1), PV = 1 << (BV - 1), NS = PK + 1;
-  // token warps: TS sets of four (one per TMEM lane quarter); set s handles HPT query heads
-  // from head s * HPT (a second set, warps 16-19, when a KV head carries 8 or more)
-  static constexpr int TS = GP >= 8 ? 2 : 1;
+  // token warps: TS = 2 sets of four (one warp per TMEM lane quarter); set s handles the HPT
+  // query heads from head s * HPT (set 0 is warps 0-3, set 1 warps 16-19).  Two sets halve
+  // each token thread's chain of per-head work on every page, which is the longest chain of
+  // the per-page loop.
+  static constexpr int TS = 2;
   static constexpr int HPT = GP / TS;
   static constexpr int WARPS = kWarpsBase + 4 * (TS - 1);
   static constexpr int THREADS = 32 * WARPS;
@@ -199,6 +204,8 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
   constexpr int D = 128, NS = C::NS, PK = C::PK, PV = C::PV, BK = C::BK, BV = C::BV, NBUF = C::NBUF;
   constexpr int NSC = C::NSC, NVC = C::NVC, NHALF = C::NHALF, DSB = C::DSB, NPW = C::NPW, AVB = C::AVB;
   constexpr int TS = C::TS, HPT = C::HPT, kThreads = C::THREADS, kWarps = C::WARPS, TNT = 128 * TS;
+  // TMEM access widths of the split token warps: this set's score columns, value columns
+  constexpr int CKS = 4 * HPT < 16 ? 4 * HPT : 16, CKV = NPW * HPT < 8 ? NPW * HPT : 8;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint8_t* s_pages = smem + C::OFF_PAGES;
   uint8_t* s_as = smem + C::OFF_AS;
@@ -567,198 +574,11 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
           if (lane == 0) mbar_arrive(&av_ready[x]);
         }
       } else if (warp < 4 || warp >= kWarpsBase) {
-      if constexpr (TS == 1) {
-        // one set of token warps (heads per KV head <= 4)
-        // ============ token warps (lane = token): logits, lazy softmax, weight operand ============
-        float m_run[GP], l_part[GP], c_part[GP], g_part[GP];
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-          m_run[h] = -INFINITY;
-          l_part[h] = c_part[h] = g_part[h] = 0.f;
-        }
-        float n_ref = 0.f;
-        for (int p = 0; p < n_pages; ++p) {
-          const uint32_t g = pg_base + p, x = g & 1, db = DSB == 2 ? x : 0;
-          const uint8_t* pgp = pg_ptr(p);
-          wait_k(&s_full[ring_slot(p)], ring_use(p));
-          const int nvalid = min(128, seq_len - (p_lo + p) * 128);
-          const bool valid = row < nvalid;
-          const float nk = valid ? reinterpret_cast<const float*>(pgp + PL::off_nk)[row] : 0.f;
-          const float gmv = valid ? reinterpret_cast<const float*>(pgp + PL::off_gamma)[row] : 0.f;
-          const float nvt = valid ? reinterpret_cast<const float*>(pgp + PL::off_nv)[row] : 0.f;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_empty[ring_slot(p)]);
-          wait_k(&s_fin[x], g >> 1);        // every score MMA of page p is done
-          tc_fence_after();
-          float ds[NSC];
-#pragma unroll
-          for (int c0 = 0; c0 < NSC; c0 += 16) {
-            uint32_t r[16];
-            tmem_ld16(tl + C::TD_S + db * C::DS_COLS + c0, r);
-            tc_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) ds[c0 + i] = __uint_as_float(r[i]);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ds_free[x]);
-          float lg[GP];
-          int ovf = nvt > n_ref;
-#pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            // folded per-head constants (set-up): logit = nk (mse ak + bk) + gamma (qjl aq + bq)
-            const float4 hc = *reinterpret_cast<const float4*>(s_head + h * 8);
-            const float* dk = ds + 4 * h;
-            const float* dq = ds + NHALF + 4 * h;
-            const float mse = fmaf(0.000244140625f, dk[3], fmaf(0.00390625f, dk[2], fmaf(0.0625f, dk[1], dk[0])));
-            const float qjl = fmaf(0.000244140625f, dq[3], fmaf(0.00390625f, dq[2], fmaf(0.0625f, dq[1], dq[0])));
-            const float l = fmaf(nk, fmaf(mse, hc.x, hc.y), gmv * fmaf(qjl, hc.z, hc.w));
-            lg[h] = (valid && h < G) ? l : -INFINITY;
-            if (a.logits && valid && h < G)
-              a.logits[((size_t)b * a.q_heads + (size_t)kvh * G + h) * a.max_tokens + (size_t)(p_lo + p) * 128 + row] = l;
-            if (lg[h] > m_run[h] + kTau) ovf = 1;
-          }
-          float fh[GP];
-#pragma unroll
-          for (int h = 0; h < GP; ++h) fh[h] = 1.f;
-          bool rescale = false;
-          if (t_vote_or<128>(ovf)) {
-#pragma unroll
-            for (int h = 0; h <= GP; ++h) {
-              float mx = h < GP ? lg[h] : nvt;
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-              if (lane == 0) s_red[warp * (GP + 1) + h] = mx;
-            }
-            t_sync<128>();
-            float nvmax = 0.f;
-            for (int w2 = 0; w2 < 4; ++w2) nvmax = fmaxf(nvmax, s_red[w2 * (GP + 1) + GP]);
-            const float n_new = nvmax > n_ref ? 1.25f * nvmax : n_ref;
-#pragma unroll
-            for (int h = 0; h < GP; ++h) {
-              float mx = -INFINITY;
-              for (int w2 = 0; w2 < 4; ++w2) mx = fmaxf(mx, s_red[w2 * (GP + 1) + h]);
-              const float m_new = fmaxf(m_run[h], mx);
-              const float alpha = (m_run[h] == -INFINITY) ? 0.f : __expf(m_run[h] - m_new);
-              fh[h] = (n_ref > 0.f) ? alpha * (n_ref / n_new) : 0.f;
-              l_part[h] *= alpha;
-              c_part[h] *= fh[h];
-              g_part[h] *= fh[h];
-              m_run[h] = m_new;
-            }
-            n_ref = n_new;
-            rescale = p > 0;
-            t_sync<128>();   // s_red reads done
-          }
-          if (p == 0) {
-            // a new segment: the flushed total starts at zero (the previous epilogue has read it)
-            uint32_t z[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) z[i] = 0u;
-#pragma unroll 1
-            for (int c0 = 0; c0 < PV * NVC; c0 += 16) tmem_st16(tl + C::TD_ACC + c0, z);
-            tc_wait_st();
-          }
-          const bool flush = p > 0 && p % kFlush == 0;
-          if (rescale || flush) {
-            // D_v holds exactly the pages of this stretch before p once the value MMAs of page
-            // p-1 are done; this warp handles its lane quarter (32 coordinates): on a flush
-            // D_acc = (D_acc + D_v) f, otherwise D_acc *= f and D_v *= f (f = 1 without rescale)
-            wait_k(&v_fin[(g - 1) & 1], (g - 1) >> 1);
-            tc_fence_after();
-#pragma unroll 1
-            for (int c0 = 0; c0 < PV * NVC; c0 += 16) {
-              uint32_t rv[16], ra[16];
-              tmem_ld16(tl + C::TD_V + c0, rv);
-              tmem_ld16(tl + C::TD_ACC + c0, ra);
-              tc_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int h = ((c0 + i) % NVC) / NPW;
-                float fv = 1.f;
-#pragma unroll
-                for (int hh = 0; hh < GP; ++hh) fv = hh == h ? fh[hh] : fv;
-                const float dv = __uint_as_float(rv[i]), da = __uint_as_float(ra[i]);
-                ra[i] = __float_as_uint(flush ? (da + dv) * fv : da * fv);
-                rv[i] = __float_as_uint(dv * fv);
-              }
-              tmem_st16(tl + C::TD_ACC + c0, ra);
-              if (!flush) tmem_st16(tl + C::TD_V + c0, rv);
-            }
-            tc_wait_st();
-          }
-          // softmax weights -> two e4m3 pieces per head; the byte for row n = 2h + piece
-          const float xs = nvt * (n_ref > 0.f ? 1.f / n_ref : 0.f) * v_igamma * kSB;
-          uint32_t wb[NVC / 4];
-#pragma unroll
-          for (int i = 0; i < NVC / 4; ++i) wb[i] = 0u;
-          // two heads per conversion: word h/2 holds rows 2h..2h+3 = [hi(h), lo(h), hi(h+1), lo(h+1)]
-#pragma unroll
-          for (int h = 0; h < GP; h += 2) {
-            const float p0 = lg[h] == -INFINITY ? 0.f : __expf(lg[h] - m_run[h]);
-            const float p1 = lg[h + 1] == -INFINITY ? 0.f : __expf(lg[h + 1] - m_run[h + 1]);
-            l_part[h] += p0;
-            l_part[h + 1] += p1;
-            const float x0 = p0 * xs, x1 = p1 * xs;
-            const uint32_t hi2 = cvt_e4m3x2(x1, x0);
-            const float2 hf = e4m3x2_to_f2(hi2);
-            const uint32_t lo2 = cvt_e4m3x2(16.f * (x1 - hf.y), 16.f * (x0 - hf.x));
-            const float2 lf = e4m3x2_to_f2(lo2);
-            const float b0 = fmaf(0.0625f, lf.x, hf.x), b1 = fmaf(0.0625f, lf.y, hf.y);
-            c_part[h] = fmaf(v_beta, b0, c_part[h]);
-            c_part[h + 1] = fmaf(v_beta, b1, c_part[h + 1]);
-            g_part[h] = fmaf(v_gamma, b0, g_part[h]);
-            g_part[h + 1] = fmaf(v_gamma, b1, g_part[h + 1]);
-            wb[h >> 1] = __byte_perm(hi2, lo2, 0x5140);
-          }
-          // B_v buffer of page p: its previous user, the value MMA of page p-2, must be done
-          if (p >= 2) wait_k(&v_fin[g & 1], (g >> 1) - 1);
-          uint8_t* bvb = s_bv + (g & 1) * C::BV_BYTES;
-          const int e = lane & 3, base = lane & ~3;
-          const int k0 = 32 * ((row >> 2) & 3) + 4 * (row >> 4);   // K byte of token 4i
-#pragma unroll
-          for (int r4 = 0; r4 < NVC / 4; ++r4) {
-            const uint32_t w0 = __shfl_sync(0xffffffffu, wb[r4], base + 0);
-            const uint32_t w1 = __shfl_sync(0xffffffffu, wb[r4], base + 1);
-            const uint32_t w2 = __shfl_sync(0xffffffffu, wb[r4], base + 2);
-            const uint32_t w3 = __shfl_sync(0xffffffffu, wb[r4], base + 3);
-            const uint32_t sel = (uint32_t)e | ((uint32_t)(e + 4) << 4);
-            const uint32_t t01 = __byte_perm(w0, w1, sel), t23 = __byte_perm(w2, w3, sel);
-            *reinterpret_cast<uint32_t*>(bvb + canon_off(4 * r4 + e, k0, 128)) = __byte_perm(t01, t23, 0x5410);
-          }
-          fence_proxy_async();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bv_ready[g & 1]);
-        }
-        // per-head sums of this segment
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-          float v3[3] = {l_part[h], c_part[h], g_part[h]};
-#pragma unroll
-          for (int c = 0; c < 3; ++c) {
-            float v = v3[c];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) s_red[(warp * (GP + 1) + h) * 3 + c] = v;
-          }
-        }
-        if (tid == 0) s_f[0] = n_ref;
-        // partial record head part (m, l)
-        t_sync<128>();
-        if (tid < GP && tid < G) {
-          float l_tot = 0.f;
-          for (int w2 = 0; w2 < 4; ++w2) l_tot += s_red[(w2 * (GP + 1) + tid) * 3];
-          float* rh = rec + (size_t)tid * (2 + D);
-          rh[0] = m_run[tid];
-          rh[1] = l_tot;
-        }
-      } else {
         // ============ token warps (lane = token): logits, lazy softmax, weight operand ============
         // set ts of TS handles heads h0 .. h0 + HPT - 1; it owns their D_s columns, their D_v
         // and D_acc columns and their B_v rows, so the sets never write the same word
         const int twarp = warp < 4 ? warp : 4 + (warp - kWarpsBase);   // 0 .. 4 TS - 1
-        const int ts = TS == 1 ? 0 : twarp >> 2, h0 = ts * HPT;   // compile-time 0 with one set
+        const int ts = twarp >> 2, h0 = ts * HPT;
         float m_run[HPT], l_part[HPT], c_part[HPT], g_part[HPT];
 #pragma unroll
         for (int h = 0; h < HPT; ++h) {
@@ -781,13 +601,13 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
           tc_fence_after();
           float dsk[4 * HPT], dsq[4 * HPT];   // this set's key-term and sign-term columns
 #pragma unroll
-          for (int c0 = 0; c0 < 4 * HPT; c0 += 16) {
-            uint32_t r[16], rq[16];
-            tmem_ld16(tl + C::TD_S + db * C::DS_COLS + 4 * h0 + c0, r);
-            tmem_ld16(tl + C::TD_S + db * C::DS_COLS + NHALF + 4 * h0 + c0, rq);
+          for (int c0 = 0; c0 < 4 * HPT; c0 += CKS) {
+            uint32_t r[CKS], rq[CKS];
+            tmem_ldn<CKS>(tl + C::TD_S + db * C::DS_COLS + 4 * h0 + c0, r);
+            tmem_ldn<CKS>(tl + C::TD_S + db * C::DS_COLS + NHALF + 4 * h0 + c0, rq);
             tc_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < CKS; ++i) {
               dsk[c0 + i] = __uint_as_float(r[i]);
               dsq[c0 + i] = __uint_as_float(rq[i]);
             }
@@ -847,12 +667,12 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
           // this set's columns of each plane accumulator: pl NVC + NPW h0 .. + NPW HPT
           if (p == 0) {
             // a new segment: the flushed total starts at zero (the previous epilogue has read it)
-            uint32_t z[8];
+            uint32_t z[CKV];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) z[i] = 0u;
+            for (int i = 0; i < CKV; ++i) z[i] = 0u;
 #pragma unroll 1
             for (int pl = 0; pl < PV; ++pl)
-              for (int co = 0; co < NPW * HPT; co += 8) tmem_st8(tl + C::TD_ACC + pl * NVC + NPW * h0 + co, z);
+              for (int co = 0; co < NPW * HPT; co += CKV) tmem_stn<CKV>(tl + C::TD_ACC + pl * NVC + NPW * h0 + co, z);
             tc_wait_st();
           }
           const bool flush = p > 0 && p % kFlush == 0;
@@ -865,21 +685,21 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
 #pragma unroll 1
             for (int pl = 0; pl < PV; ++pl) {
 #pragma unroll
-              for (int co = 0; co < NPW * HPT; co += 8) {
+              for (int co = 0; co < NPW * HPT; co += CKV) {
                 const uint32_t col = pl * NVC + NPW * h0 + co;
-                uint32_t rv[8], ra[8];
-                tmem_ld8(tl + C::TD_V + col, rv);
-                tmem_ld8(tl + C::TD_ACC + col, ra);
+                uint32_t rv[CKV], ra[CKV];
+                tmem_ldn<CKV>(tl + C::TD_V + col, rv);
+                tmem_ldn<CKV>(tl + C::TD_ACC + col, ra);
                 tc_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < CKV; ++i) {
                   const float fv = fh[(co + i) / NPW];
                   const float dv = __uint_as_float(rv[i]), da = __uint_as_float(ra[i]);
                   ra[i] = __float_as_uint(flush ? (da + dv) * fv : da * fv);
                   rv[i] = __float_as_uint(dv * fv);
                 }
-                tmem_st8(tl + C::TD_ACC + col, ra);
-                if (!flush) tmem_st8(tl + C::TD_V + col, rv);
+                tmem_stn<CKV>(tl + C::TD_ACC + col, ra);
+                if (!flush) tmem_stn<CKV>(tl + C::TD_V + col, rv);
               }
             }
             tc_wait_st();
@@ -955,7 +775,6 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
           rh[0] = mv;
           rh[1] = l_tot;
         }
-      }
       }
     }
     if (n_pages == 0 && warp == 0 && tid < GP && tid < G) {
