@@ -47,8 +47,9 @@ using namespace dev;
 using dmma::Params;
 
 // Warp numbering: every 4-warp role starts at a multiple of 4 (warp % 4 is the TMEM lane
-// quarter a warp may access).  Measured on B300: with the issuers and waiters in warps 0-3
-// instead of 12-15 the kernel ran 2-12% slower.
+// quarter a warp may access).  Measured on B300: the order of the 4-warp roles makes no
+// difference (within 0.5%); with the issuers and waiters in warps 0-3 instead of 12-15 the
+// kernel ran 2-12% slower.
 constexpr int kWarpT = 0;             // token warps, first set (4)
 constexpr int kWarpK = 4;             // key-plane warps (4)
 constexpr int kWarpV = 8;             // value-plane warps (4); epilogue
@@ -56,7 +57,8 @@ constexpr int kWarpS = 12;            // issues the score MMAs
 constexpr int kWarpM = 13;            // issues the value MMAs
 constexpr int kWarpWS = 14;           // waits for the score operands, hands them to kWarpS
 constexpr int kWarpWM = 15;           // waits for the value operands, hands them to kWarpM; page ring
-constexpr int kWarpsBase = 16;        // token warps, second set (4)
+constexpr int kWarpT2 = 16;           // token warps, second set (4)
+constexpr int kWarpsAll = 20;
 static_assert(kWarpT == 0, "the segment's n_ref is stored by thread 0 as the first token thread");
 constexpr int kL2Ahead = 12;
 constexpr float kTau = 3.0f;          // lazy-maximum threshold (natural-log units)
@@ -82,7 +84,7 @@ struct Cfg {
   // the per-page loop.
   static constexpr int TS = 2;
   static constexpr int HPT = GP / TS;
-  static constexpr int WARPS = kWarpsBase + 4 * (TS - 1);
+  static constexpr int WARPS = kWarpsAll;
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int NQP = 4;                          // e4m3 pieces per query coordinate
   static constexpr int NHALF = rnd(NQP * GP, 8);       // score columns: [key term | sign term]
@@ -579,11 +581,11 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
           __syncwarp();
           if (lane == 0) mbar_arrive(&av_ready[x]);
         }
-      } else if ((warp >= kWarpT && warp < kWarpT + 4) || warp >= kWarpsBase) {
+      } else if ((warp >= kWarpT && warp < kWarpT + 4) || (warp >= kWarpT2 && warp < kWarpT2 + 4)) {
         // ============ token warps (lane = token): logits, lazy softmax, weight operand ============
         // set ts of TS handles heads h0 .. h0 + HPT - 1; it owns their D_s columns, their D_v
         // and D_acc columns and their B_v rows, so the sets never write the same word
-        const int twarp = warp < kWarpsBase ? warp - kWarpT : 4 + (warp - kWarpsBase);   // 0 .. 4 TS - 1
+        const int twarp = (warp >= kWarpT2 && warp < kWarpT2 + 4) ? 4 + (warp - kWarpT2) : warp - kWarpT;   // 0 .. 7
         const int ts = twarp >> 2, h0 = ts * HPT;
         float m_run[HPT], l_part[HPT], c_part[HPT], g_part[HPT];
 #pragma unroll
