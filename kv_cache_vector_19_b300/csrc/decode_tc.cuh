@@ -344,6 +344,9 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
       s_q[e] = v;
     }
     for (int e = tid; e < GP * 8; e += kThreads) s_head[e] = 0.f;
+    // both B_v buffers start at zero: the padding rows past 2 GP (N is at least 16) stay zero,
+    // the token warps rewrite only the rows of their heads on every page
+    for (int e = tid; e < 2 * C::BV_BYTES / 4; e += kThreads) reinterpret_cast<uint32_t*>(s_bv)[e] = 0u;
     __syncthreads();
     for (int hh = warp; hh < GP; hh += kWarps) {   // power-of-two scales: largest operand <= 224
       float mk = 0.f, mq = 0.f;
@@ -739,19 +742,17 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
           uint8_t* bvb = s_bv + (g & 1) * C::BV_BYTES;
           const int e = lane & 3, base = lane & ~3;
           const int k0 = 32 * ((row >> 2) & 3) + 4 * (row >> 4);   // K byte of token 4i
-          // this set's words (rows 4 w .. 4 w + 3); the last set also writes the zero padding rows
-          constexpr int NW_PAD = NVC / 4 - GP / 2;
+          // this set's words (rows 4 w .. 4 w + 3)
 #pragma unroll
-          for (int r4 = 0; r4 < HPT / 2 + NW_PAD; ++r4) {
-            if (r4 >= HPT / 2 && ts != TS - 1) break;
-            const uint32_t wv = r4 < HPT / 2 ? wb[r4 < HPT / 2 ? r4 : 0] : 0u;
+          for (int r4 = 0; r4 < HPT / 2; ++r4) {
+            const uint32_t wv = wb[r4];
             const uint32_t w0 = __shfl_sync(0xffffffffu, wv, base + 0);
             const uint32_t w1 = __shfl_sync(0xffffffffu, wv, base + 1);
             const uint32_t w2 = __shfl_sync(0xffffffffu, wv, base + 2);
             const uint32_t w3 = __shfl_sync(0xffffffffu, wv, base + 3);
             const uint32_t sel = (uint32_t)e | ((uint32_t)(e + 4) << 4);
             const uint32_t t01 = __byte_perm(w0, w1, sel), t23 = __byte_perm(w2, w3, sel);
-            const int word = r4 < HPT / 2 ? h0 / 2 + r4 : GP / 2 + (r4 - HPT / 2);
+            const int word = h0 / 2 + r4;
             *reinterpret_cast<uint32_t*>(bvb + canon_off(4 * word + e, k0, 128)) = __byte_perm(t01, t23, 0x5410);
           }
           fence_proxy_async();
