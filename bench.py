@@ -35,7 +35,7 @@ METRIC = "compressed-KV decode GB/s & % HBM roofline; quantize Mtokens/s (d=128,
 UNIT = "GB/s"
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode_tc_kernel<3,4> launch on this
 # workload (ncu, one launch after warm-up); None whenever that kernel has changed since.
-DECODE_TRAFFIC_BYTES = 461369600
+DECODE_TRAFFIC_BYTES = 461296640
 
 
 def bpt(d, b, m):
