@@ -26,7 +26,8 @@ Modules:
     rng       SplitMix64 counter stream and Box-Muller Gaussians (published definitions)
     rotation  Haar rotation Pi (QR of a Gaussian matrix, sign-fixed) and Gaussian S
     codebook  Lloyd-Max quantizer for one coordinate of a random unit vector in R^d
-    quant     per-vector quantization of keys (MSE + QJL) and values (MSE)
-    pagefmt   bit-exact packer / unpacker of the compressed page format (version 1)
+    quant     per-vector quantization of keys (MSE + QJL, or MSE only) and values (MSE)
+    pagefmt   bit-exact packer / unpacker of the compressed page formats (version 1, and
+              version 2 with separate key / value widths and optional QJL)
     decode    decode attention over the compressed cache (two equivalent routes)
 """

@@ -12,6 +12,9 @@ Readings: logits are scaled by 1/sqrt(d); no mask other than t < seq_len; query 
 reads kv head floor(h / G) with G = Hq / Hkv (consecutive grouping); an empty sequence
 (seq_len = 0) yields an all-zero output.
 
+Keys without the QJL stage (tok_k["sigma"] is None; [3BITS] "Python + HuggingFace" and its
+remark that the llama.cpp forks switch QJL off) score by the Lloyd-Max term alone.
+
 Two routes are given.  Route A reconstructs every key and value in the original frame
 (plain definition).  Route B works in the rotated frame (q~ = Pi q, q_s = S q, output
 rotated back once by Pi^T); it is mathematically identical and serves as an internal
@@ -35,7 +38,7 @@ def attend_route_a(q, tok_k, tok_v, Pi, S, cb_k, cb_v):
     T = len(tok_k["n"])
     if T == 0:
         return np.zeros(d), np.zeros(0)
-    khat = quant.reconstruct_keys(tok_k["idx"], tok_k["n"], tok_k["sigma"], tok_k["gamma"], Pi, S, cb_k[0])
+    khat = quant.reconstruct_keys_any(tok_k, Pi, S, cb_k[0])
     logits = khat @ np.asarray(q, dtype=np.float64) / np.sqrt(d)
     p = _softmax(logits)
     vhat = quant.reconstruct_values(tok_v["idx"], tok_v["n"], Pi, cb_v[0])
@@ -45,17 +48,19 @@ def attend_route_a(q, tok_k, tok_v, Pi, S, cb_k, cb_v):
 def attend_route_b(q, tok_k, tok_v, Pi, S, cb_k, cb_v):
     """Rotated-frame evaluation of the same quantities as ``attend_route_a``."""
     d = Pi.shape[0]
-    m = S.shape[0]
     T = len(tok_k["n"])
     if T == 0:
         return np.zeros(d), np.zeros(0)
     q = np.asarray(q, dtype=np.float64)
     qr = Pi @ q
-    qs = S @ q
     nk = np.asarray(tok_k["n"], dtype=np.float64)
-    gm = np.asarray(tok_k["gamma"], dtype=np.float64)
     mse = nk * (np.asarray(cb_k[0])[tok_k["idx"]] @ qr)
-    qjl = gm * quant.QJL_CONST / m * ((2.0 * np.asarray(tok_k["sigma"], dtype=np.float64) - 1.0) @ qs)
+    qjl = 0.0
+    if tok_k.get("sigma") is not None:
+        m = S.shape[0]
+        qs = S @ q
+        gm = np.asarray(tok_k["gamma"], dtype=np.float64)
+        qjl = gm * quant.QJL_CONST / m * ((2.0 * np.asarray(tok_k["sigma"], dtype=np.float64) - 1.0) @ qs)
     logits = (mse + qjl) / np.sqrt(d)
     p = _softmax(logits)
     nv = np.asarray(tok_v["n"], dtype=np.float64)

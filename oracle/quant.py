@@ -66,6 +66,14 @@ def quantize_keys(X, Pi, S, cb_k):
                 sigma=sigma, yhat=yhat, z=z, n64=n, gamma64=gamma)
 
 
+def quantize_keys_mse(X, Pi, cb_k):
+    """Keys without the QJL stage ([3BITS] "Python + HuggingFace": the stage-1 quantizer
+    returns indices and norms): dict(idx, n (fp32), sigma None, gamma None, plus yhat)."""
+    c, t = cb_k
+    idx, n, yhat = mse_stage(X, Pi, c, t)
+    return dict(idx=idx, n=n.astype(np.float32), sigma=None, gamma=None, yhat=yhat, n64=n)
+
+
 def quantize_values(X, Pi, cb_v):
     """Values: dict(idx, n (fp32), plus fp64 yhat)."""
     c, t = cb_v
@@ -85,6 +93,14 @@ def reconstruct_keys(idx, n, sigma, gamma, Pi, S, centroids):
     signs = 2.0 * np.asarray(sigma, dtype=np.float64) - 1.0
     g = np.asarray(gamma, dtype=np.float64)
     return dequant_mse(idx, n, Pi, centroids) + (g * QJL_CONST / m)[:, None] * (signs @ S)
+
+
+def reconstruct_keys_any(tok_k, Pi, S, centroids):
+    """khat for keys with the QJL stage (sigma present) or without it (sigma None: stage 1
+    only, khat = n Pi^T c[idx])."""
+    if tok_k.get("sigma") is None:
+        return dequant_mse(tok_k["idx"], tok_k["n"], Pi, centroids)
+    return reconstruct_keys(tok_k["idx"], tok_k["n"], tok_k["sigma"], tok_k["gamma"], Pi, S, centroids)
 
 
 def reconstruct_values(idx, n, Pi, centroids):
