@@ -92,7 +92,7 @@ def test_decode_small(d, b, G):
     ("mma", 64, 2, 1), ("mma", 128, 3, 4), ("mma", 128, 4, 8), ("mma", 128, 3, 16), ("mma", 128, 2, 3),
     ("mma", 128, 5, 2), ("mma", 256, 4, 1),
     ("tc", 128, 3, 4), ("tc", 128, 3, 8), ("tc", 128, 3, 16), ("tc", 128, 2, 3), ("tc", 128, 2, 16),
-    ("tc", 128, 3, 1)])
+    ("tc", 128, 3, 1), ("tc", 128, 3, 2), ("tc", 128, 3, 6), ("tc", 128, 2, 12)])
 def test_decode_small_each_kernel(path, d, b, G):
     _check_decode(d, b, G, path)
 
