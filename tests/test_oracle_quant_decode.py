@@ -145,6 +145,38 @@ def test_hand_built_page_d32_b2():
     assert np.array_equal(words, expected)
 
 
+@pytest.mark.parametrize("name", ["page_d128_b3.json", "page_d256_b2.json"])
+def test_hand_built_pages_wide(name):
+    """Hand-derived words at d = 128 and 256, where the key/sign map's 2*kb term and its
+    D-dependent stride (2*D/32 per c) take values that d = 32 never reaches."""
+    g = json.load(open(os.path.join(HERE, "golden", name)))
+    d, b, m, P = g["d"], g["b"], g["m"], 128
+    arrays = dict(kidx=np.zeros((P, d), dtype=np.int64), sigma=np.zeros((P, m), dtype=np.uint8),
+                  vidx=np.zeros((P, d), dtype=np.int64), nk=np.zeros(P, dtype=np.float32),
+                  gamma=np.zeros(P, dtype=np.float32), nv=np.zeros(P, dtype=np.float32))
+    for inp in g["inputs"]:
+        a = arrays[inp["field"]]
+        if a.ndim == 1:
+            a[inp["slot"]] = inp["value"]
+        elif "coords" in inp:
+            lo, hi = inp["coords"]
+            a[inp["slot"], lo:hi + 1] = inp["value"]
+        else:
+            a[inp["slot"], inp["coord"]] = inp["value"]
+    buf = pagefmt.pack_page(d, b, m, arrays["kidx"], arrays["sigma"], arrays["nk"], arrays["gamma"],
+                            arrays["vidx"], arrays["nv"])
+    assert len(buf) == g["page_bytes"]
+    words = buf.view("<u4")
+    expected = np.zeros_like(words)
+    for case in g["cases"]:
+        expected[case["offset"] // 4] = int(case["u32"], 16)
+    assert np.array_equal(words, expected), np.nonzero(words != expected)
+    # and the unpacker reads the hand-derived page back to the same fields
+    u = pagefmt.unpack_page(d, b, m, expected.view(np.uint8))
+    for key, a in arrays.items():
+        assert np.array_equal(np.asarray(u[key]), a), key
+
+
 def _random_tokens(p, T, rs, scale=1.0):
     Xk = _bf16_like(rs.standard_normal((T, p.d)) * scale)
     Xv = _bf16_like(rs.standard_normal((T, p.d)))

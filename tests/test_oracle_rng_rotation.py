@@ -1,4 +1,7 @@
 """Pins for the oracle's random streams and seeded matrices (CPU only)."""
+import json
+import os
+
 import numpy as np
 import pytest
 
@@ -9,6 +12,21 @@ def test_splitmix64_known_answers():
     # Published reference outputs of splitmix64.c (Vigna) started from state 0.
     out = rng.splitmix64(0, 3)
     assert [int(x) for x in out] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+def test_splitmix64_fourth_output_and_gaussian_known_answers():
+    """Box-Muller pairing pinned by known answers (tests/golden/gaussians_seed0.json): the
+    first four published SplitMix64 outputs of state 0, the uniforms they give and the
+    four Gaussians of stream 0.  Swapping cos and sin, taking u1 instead of 1 - u1, or
+    pairing other than consecutive outputs changes these values."""
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "gaussians_seed0.json")))
+    assert [int(x) for x in rng.splitmix64(0, 4)] == [int(x, 16) for x in g["splitmix64_outputs"]]
+    u = rng.uniforms(0, 4)
+    assert [float(x) for x in u] == [g["pairs"][0]["u1"], g["pairs"][0]["u2"], g["pairs"][1]["u1"], g["pairs"][1]["u2"]]
+    got = rng.gaussians(0, 4)
+    assert np.max(np.abs(got - np.array(g["gaussians"]))) <= g["tolerance"]
+    # an odd count is the prefix of the even one
+    assert np.array_equal(rng.gaussians(0, 3), got[:3])
 
 
 def test_splitmix64_is_counter_based():
