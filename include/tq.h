@@ -95,8 +95,10 @@ enum {
   TQ_DECODE_SIMT = 1, /* CUDA cores: every d, bits and group size                          */
   TQ_DECODE_MMA = 2,  /* fp8 mma.sync over bit planes: d in {64,128,256}; how many query   */
                       /* heads per kv head it takes shrinks as d and bits grow (registers) */
-  TQ_DECODE_TC = 3    /* tcgen05 over bit planes, operands in tensor memory: d == 128,     */
-                      /* bits in {2,3}, group size <= 16                                   */
+  TQ_DECODE_TC = 3,   /* tcgen05 over bit planes, e4m3 operands: d == 128, bits in {2,3},  */
+                      /* group size <= 16                                                   */
+  TQ_DECODE_TC4 = 4   /* tcgen05 over signed bit planes, block-scaled e2m1 operands        */
+                      /* (kind::mxf4): d == 128, bits in {2,3}, group size <= 8            */
 };
 
 /* ---- host-only set-up (no GPU needed) ------------------------------------------- */

@@ -23,8 +23,9 @@ TQ_EBOUNDS = -5
 TQ_ENOMEM = -6
 TQ_ENOTCONV = -7
 TQ_ESCRATCH = -8
-TQ_DECODE_AUTO, TQ_DECODE_SIMT, TQ_DECODE_MMA, TQ_DECODE_TC = 0, 1, 2, 3
-DECODE_PATHS = {"auto": TQ_DECODE_AUTO, "simt": TQ_DECODE_SIMT, "mma": TQ_DECODE_MMA, "tc": TQ_DECODE_TC}
+TQ_DECODE_AUTO, TQ_DECODE_SIMT, TQ_DECODE_MMA, TQ_DECODE_TC, TQ_DECODE_TC4 = 0, 1, 2, 3, 4
+DECODE_PATHS = {"auto": TQ_DECODE_AUTO, "simt": TQ_DECODE_SIMT, "mma": TQ_DECODE_MMA, "tc": TQ_DECODE_TC,
+                "tc4": TQ_DECODE_TC4}
 PAGE_TOKENS = 128
 # kernels one call launches (the benchmark reports launch counts from these)
 QUANTIZE_LAUNCHES = 1
@@ -208,7 +209,7 @@ class Context:
             self.set_decode_path(decode_path)
 
     def set_decode_path(self, path):
-        """'auto', 'simt', 'mma' or 'tc' (TQ_DECODE_*); query workspace sizes afterwards."""
+        """'auto', 'simt', 'mma', 'tc' or 'tc4' (TQ_DECODE_*); query workspace sizes afterwards."""
         code = DECODE_PATHS[path] if isinstance(path, str) else int(path)
         _check("tq_ctx_set_decode_path", lib().tq_ctx_set_decode_path(self._ctx, code))
         self.decode_path = path

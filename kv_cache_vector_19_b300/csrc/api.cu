@@ -175,6 +175,7 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
     if (rc == TQ_OK) rc = prepare_quantize_simt(c);
     if (rc == TQ_OK) rc = tq::prepare_decode_mma(c);
     if (rc == TQ_OK) rc = tq::prepare_decode_tc(c);
+    if (rc == TQ_OK) rc = tq::prepare_decode_f4(c);
     if (rc == TQ_OK && d == 128) {
       std::vector<double> sp((size_t)m * d);   // S'[i][j] row-major
       for (int i = 0; i < m; ++i)
@@ -252,6 +253,7 @@ extern "C" int tq_ctx_set_decode_path(tq_ctx* ctx, int path) {
       if (ctx->d != 64 && ctx->d != 128 && ctx->d != 256) return TQ_EUNSUPPORTED;
       break;
     case TQ_DECODE_TC:
+    case TQ_DECODE_TC4:
       if (ctx->d != 128 || (ctx->bits != 2 && ctx->bits != 3)) return TQ_EUNSUPPORTED;
       break;
     default:
@@ -266,9 +268,10 @@ namespace {
 // Kernel a decode call takes: TQ_DECODE_SIMT / _MMA / _TC, or TQ_EUNSUPPORTED.  The bit-plane
 // kernels share one launch plan (mp).
 int decode_kernel_for(const tq_ctx* ctx, int batch, int q_heads, int kv_heads, int max_tokens, tq::MmaPlan* mp) {
-  tq::MmaPlan pm, pt;
+  tq::MmaPlan pm, pt, pf;
   const bool mma_ok = tq::plan_decode_mma(ctx, batch, q_heads, kv_heads, max_tokens, &pm);
   const bool tc_ok = tq::plan_decode_tc(ctx, batch, q_heads, kv_heads, max_tokens, &pt);
+  const bool f4_ok = tq::plan_decode_f4(ctx, batch, q_heads, kv_heads, max_tokens, &pf);
   int kern = TQ_EUNSUPPORTED;
   switch (ctx->decode_path) {
     case TQ_DECODE_SIMT:
@@ -280,12 +283,17 @@ int decode_kernel_for(const tq_ctx* ctx, int batch, int q_heads, int kv_heads, i
     case TQ_DECODE_TC:
       if (tc_ok) kern = TQ_DECODE_TC;
       break;
+    case TQ_DECODE_TC4:
+      if (f4_ok) kern = TQ_DECODE_TC4;
+      break;
     default:
-      if (tc_ok && (!mma_ok || tq::decode_tc_preferred(ctx, q_heads, kv_heads))) kern = TQ_DECODE_TC;
+      if (f4_ok) kern = TQ_DECODE_TC4;
+      else if (tc_ok && (!mma_ok || tq::decode_tc_preferred(ctx, q_heads, kv_heads))) kern = TQ_DECODE_TC;
       else kern = mma_ok ? TQ_DECODE_MMA : TQ_DECODE_SIMT;
   }
   if (kern == TQ_DECODE_MMA) *mp = pm;
   if (kern == TQ_DECODE_TC) *mp = pt;
+  if (kern == TQ_DECODE_TC4) *mp = pf;
   return kern;
 }
 
@@ -297,7 +305,8 @@ extern "C" size_t tq_decode_workspace_bytes(const tq_ctx* ctx, int batch, int q_
   if (q_heads % kv_heads != 0) return 0;
   tq::MmaPlan mp;
   const int kern = decode_kernel_for(ctx, batch, q_heads, kv_heads, max_tokens, &mp);
-  if (kern == TQ_DECODE_MMA || kern == TQ_DECODE_TC) return tq::decode_mma_workspace(ctx, mp, batch, q_heads, kv_heads);
+  if (kern == TQ_DECODE_MMA || kern == TQ_DECODE_TC || kern == TQ_DECODE_TC4)
+    return tq::decode_mma_workspace(ctx, mp, batch, q_heads, kv_heads);
   if (kern != TQ_DECODE_SIMT) return 0;
   tq::SplitPlan sp = tq::plan_splits(batch, kv_heads, max_tokens);
   size_t rows = (size_t)batch * q_heads;
@@ -321,6 +330,9 @@ extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int 
   if (kern < 0) return kern;
   if (workspace_bytes < tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens)) return TQ_ENOMEM;
   DeviceGuard guard(ctx->device);
+  if (kern == TQ_DECODE_TC4)
+    return tq::launch_decode_f4(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
+                                workspace, stream);
   if (kern == TQ_DECODE_TC)
     return tq::launch_decode_tc(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
                                 workspace, stream);

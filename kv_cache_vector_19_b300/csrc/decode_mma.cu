@@ -305,3 +305,108 @@ int launch_decode_tc(const tq_ctx* c, const MmaPlan& pl, const float* q, int bat
 }
 
 }  // namespace tq
+
+// ---------------------------------------------------------------- tcgen05 decode, 4-bit operands (d = 128)
+#include "decode_f4.cuh"
+
+namespace tq {
+namespace {
+
+template <int BITS, int GP>
+int f4_prepare_one() {
+  using C = dtf::Cfg<BITS, GP>;
+  if constexpr (!C::SUPPORTED) {
+    return TQ_OK;
+  } else {
+    return cudaFuncSetAttribute(dtf::decode_f4_kernel<BITS, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM) == cudaSuccess
+               ? TQ_OK
+               : TQ_ECUDA;
+  }
+}
+
+int f4_gp(int group) { return group <= 4 ? 4 : group <= 8 ? 8 : 0; }
+
+template <int BITS, int GP>
+int f4_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
+                  const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws,
+                  cudaStream_t st) {
+  using C = dtf::Cfg<BITS, GP>;
+  if constexpr (!C::SUPPORTED) {
+    return TQ_EUNSUPPORTED;
+  } else {
+    constexpr int D = 128;
+    float* qr = static_cast<float*>(ws);
+    float* qs = qr + (size_t)batch * q_heads * D;
+    float* part = qs + (size_t)batch * q_heads * D;
+    launch_prologue(c, q, batch, q_heads, qr, qs, st);
+    dmma::Params a;
+    a.qr = qr;
+    a.qs = qs;
+    a.cache = static_cast<const uint8_t*>(cache);
+    a.seq_lens = seq_lens;
+    a.logits = logits;
+    a.part = part;
+    a.alpha_k = c->d_alpha_k;
+    a.alpha_v = c->d_alpha_v;
+    a.status = c->d_status;
+    a.asum_k = c->asum_k;
+    a.asum_v = c->asum_v;
+    a.batch = batch;
+    a.q_heads = q_heads;
+    a.kv_heads = kv_heads;
+    a.group = q_heads / kv_heads;
+    a.max_tokens = max_tokens;
+    a.pages_per_seq = pl.pages_per_seq;
+    a.chunk = pl.chunk;
+    a.slots = pl.slots;
+    a.total_pages = pl.total_pages;
+    dtf::decode_f4_kernel<BITS, GP><<<pl.grid, C::THREADS, C::SMEM, st>>>(a);
+    dmma::combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
+                                                                pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
+    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
+  }
+}
+
+}  // namespace
+
+bool decode_f4_supported(const tq_ctx* c, int q_heads, int kv_heads) {
+  if (c->d != 128 || q_heads % kv_heads != 0) return false;
+  const int gp = f4_gp(q_heads / kv_heads);
+  if (gp == 0) return false;
+#define TQ_S(BB, GG) \
+  if (c->bits == BB && gp == GG) return dtf::Cfg<BB, GG>::SUPPORTED;
+  TQ_S(2, 4) TQ_S(2, 8) TQ_S(3, 4) TQ_S(3, 8)
+#undef TQ_S
+  return false;
+}
+
+bool plan_decode_f4(const tq_ctx* c, int batch, int q_heads, int kv_heads, int max_tokens, MmaPlan* p) {
+  return decode_f4_supported(c, q_heads, kv_heads) && plan_pages(c->num_sms, batch, kv_heads, max_tokens, p);
+}
+
+int prepare_decode_f4(const tq_ctx* c) {
+  if (c->d != 128) return TQ_OK;
+  int rc = TQ_OK;
+#define TQ_P(BB, GG) \
+  if (rc == TQ_OK && c->bits == BB) rc = f4_prepare_one<BB, GG>();
+  TQ_P(2, 4) TQ_P(2, 8) TQ_P(3, 4) TQ_P(3, 8)
+#undef TQ_P
+  return rc;
+}
+
+int launch_decode_f4(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
+                     const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
+                     void* workspace, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int gp = f4_gp(q_heads / kv_heads);
+#define TQ_L(BB, GG)                                                                                         \
+  if (c->bits == BB && gp == GG)                                                                             \
+    return f4_launch_one<BB, GG>(c, pl, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out, \
+                                 workspace, st);
+  TQ_L(2, 4) TQ_L(2, 8) TQ_L(3, 4) TQ_L(3, 8)
+#undef TQ_L
+  return TQ_EUNSUPPORTED;
+}
+
+}  // namespace tq

@@ -166,25 +166,6 @@ __host__ __device__ __forceinline__ int slot_of_col(int w, int k, int e) {
   return 32 * (k >> 1) + 16 * (k & 1) + 4 * w + e;
 }
 
-// The words of every odd-subset ("monomial") plane of a slot row, built once per page with
-// the subset masks folded at compile time: xp[pl] = XOR of w[q] over the bits q of subset pl.
-template <int NB, int NP>
-__device__ __forceinline__ void monomial_words(const uint4 (&w)[NB], uint4 (&xp)[NP]) {
-#pragma unroll
-  for (int pl = 0; pl < NP; ++pl) {
-    uint4 x = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int q = 0; q < NB; ++q)
-      if ((mono_mask16(pl) >> q) & 1) {
-        x.x ^= w[q].x;
-        x.y ^= w[q].y;
-        x.z ^= w[q].z;
-        x.w ^= w[q].w;
-      }
-    xp[pl] = x;
-  }
-}
-
 // xp[pl] for a runtime plane index (predicated selects; keeps the plane loop rolled).
 template <int NP>
 __device__ __forceinline__ void pick_plane(const uint4 (&xp)[NP], int pl, uint32_t (&x)[4]) {

@@ -304,3 +304,73 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 
 }  // namespace dev
 }  // namespace tq
+
+namespace tq {
+namespace dev {
+
+// ---------------------------------------------------------------- 4-bit (e2m1) operands
+// Two floats -> two e2m1 nibbles in one byte (round to nearest even, saturating at +-6):
+// low nibble = lo_val.  e2m1 values: +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float hi_val, float lo_val) {
+  uint16_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}"
+      : "=h"(r)
+      : "f"(hi_val), "f"(lo_val));
+  return r;
+}
+// Two e2m1 nibbles (low nibble -> .x) back to floats.
+__device__ __forceinline__ float2 e2m1x2_to_f2(uint32_t v) {
+  uint32_t h2;
+  asm("{\n .reg .b8 t;\n cvt.u8.u16 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(h2) : "h"((uint16_t)v));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+// Instruction descriptor of kind::mxf4 (block-scaled e2m1 x e2m1 -> f32, K = 64): A and B
+// formats e2m1, K-major, N >> 3, ue8m0 scale factors, M >> 4, scale-factor ids 0.
+__host__ __device__ constexpr uint32_t make_idesc_mxf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, packed e2m1 operands (64 per 32 bytes), one scale
+// factor per 32 elements of K from tensor memory (sfa, sfb), issued by one thread.
+__device__ __forceinline__ void mma_f4_ts(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], [%1], %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_taddr),
+      "r"(a_taddr), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// The words of every odd-subset ("monomial") plane of a slot row, built once per page with
+// the subset masks folded at compile time: xp[pl] = XOR of w[q] over the bits q of subset pl.
+template <int NB, int NP>
+__device__ __forceinline__ void monomial_words(const uint4 (&w)[NB], uint4 (&xp)[NP]) {
+#pragma unroll
+  for (int pl = 0; pl < NP; ++pl) {
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int q = 0; q < NB; ++q)
+      if ((mono_mask16(pl) >> q) & 1) {
+        x.x ^= w[q].x;
+        x.y ^= w[q].y;
+        x.z ^= w[q].z;
+        x.w ^= w[q].w;
+      }
+    xp[pl] = x;
+  }
+}
+
+// A plane word w (32 bits, element k at bit k) as four words of signed e2m1 operands: output
+// word s holds, in nibble i, +1 (0x2) if bit 4i + s of w is 0 and -1 (0xA) if it is 1.
+__device__ __forceinline__ void expand_signed4(uint32_t w, uint32_t (&o)[4]) {
+  o[0] = ((w << 3) & 0x88888888u) | 0x22222222u;
+  o[1] = ((w << 2) & 0x88888888u) | 0x22222222u;
+  o[2] = ((w << 1) & 0x88888888u) | 0x22222222u;
+  o[3] = (w & 0x88888888u) | 0x22222222u;
+}
+
+}  // namespace dev
+}  // namespace tq

@@ -105,6 +105,14 @@ int prepare_decode_tc(const tq_ctx* c);
 int launch_decode_tc(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                      const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
                      void* workspace, void* stream);
+// tcgen05 decode with 4-bit (e2m1) operands: head_dim 128, b in {2, 3}, up to 8 query heads
+// per KV head; same plan, workspace and partial records as the mma.sync kernel.
+bool decode_f4_supported(const tq_ctx* c, int q_heads, int kv_heads);
+bool plan_decode_f4(const tq_ctx* c, int batch, int q_heads, int kv_heads, int max_tokens, MmaPlan* p);
+int prepare_decode_f4(const tq_ctx* c);
+int launch_decode_f4(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
+                     const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
+                     void* workspace, void* stream);
 // q~ = Pi q and q_s = S q for every (batch, query head), fp32.
 void launch_prologue(const tq_ctx* c, const float* q, int batch, int q_heads, float* qr, float* qs,
                      cudaStream_t st);

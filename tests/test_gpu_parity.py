@@ -92,7 +92,9 @@ def test_decode_small(d, b, G):
     ("mma", 64, 2, 1), ("mma", 128, 3, 4), ("mma", 128, 4, 8), ("mma", 128, 3, 16), ("mma", 128, 2, 3),
     ("mma", 128, 5, 2), ("mma", 256, 4, 1),
     ("tc", 128, 3, 4), ("tc", 128, 3, 8), ("tc", 128, 3, 16), ("tc", 128, 2, 3), ("tc", 128, 2, 16),
-    ("tc", 128, 3, 1), ("tc", 128, 3, 2), ("tc", 128, 3, 6), ("tc", 128, 2, 12)])
+    ("tc", 128, 3, 1), ("tc", 128, 3, 2), ("tc", 128, 3, 6), ("tc", 128, 2, 12),
+    ("tc4", 128, 3, 4), ("tc4", 128, 3, 8), ("tc4", 128, 2, 3), ("tc4", 128, 3, 1), ("tc4", 128, 3, 2),
+    ("tc4", 128, 2, 8), ("tc4", 128, 3, 6), ("tc4", 128, 2, 5)])
 def test_decode_small_each_kernel(path, d, b, G):
     _check_decode(d, b, G, path)
 
@@ -108,7 +110,7 @@ def test_decode_path_selection():
         assert ctx.workspace_bytes(2, 8, 2, 700) > 0
 
 
-@pytest.mark.parametrize("path", ["tc", "mma", "simt"])
+@pytest.mark.parametrize("path", ["tc4", "tc", "mma", "simt"])
 def test_decode_long_sequences_each_kernel(path):
     """Sequences of ~120 pages, so that every CTA of the bit-plane kernels streams far more
     pages than its shared-memory ring holds (ring refills, many segments), checked on two
