@@ -12,9 +12,15 @@ Printed (rank 0, one JSON line):
               phase (appends included), summed over all ranks' work / max-over-ranks time;
   quantize_mtok_s  prefill tokens (all KV heads of a token) per second;
   roofline    the decode kernel's algorithmic GB/s against the measured HBM copy peak;
-  e2e         the same metric with the step's inputs copied from pinned host memory and
-              the step's outputs read back, inside the timed region;
-  cpu_baseline  the fp64 oracle on a bounded sample of the same workload, host cores.
+  e2e         the same decode bytes over the whole step measured through the API with host
+              buffers: the prefill K/V and every decode step's inputs copied in from pinned
+              host memory, every output read back, prefill quantize and decode included;
+  cpu_baseline  the fp64 oracle on a bounded sample of the same workload, on one host thread
+              (its page unpacking is plain Python), with the figure at the BLAS pool size beside.
+
+roofline.traffic is the DRAM traffic of one decode-kernel launch from a committed ncu summary
+(profiles/), used only while the summary's recorded source fingerprint matches the kernel
+source being run; otherwise null.
 
 --impl reference times the oracle alone (there is no other implementation of this path).
 --sweep prints one line per (d, b) point of the bit/dim sweep instead.
@@ -33,9 +39,36 @@ if ROOT not in sys.path:
 
 METRIC = "compressed-KV decode GB/s & % HBM roofline; quantize Mtokens/s (d=128, b=3)"
 UNIT = "GB/s"
-# dram__bytes_read.sum + dram__bytes_write.sum of one decode_tc_kernel<3,4> launch on this
-# workload (ncu, one launch after warm-up); None whenever that kernel has changed since.
-DECODE_TRAFFIC_BYTES = 461296640
+DTYPE = ("decode: e2m1 operand pieces (signed bit planes x fixed-point / e2m1 pieces), fp32 accumulate; "
+         "quantize: bf16 hi/lo MMAs, fp32 accumulate; cache: packed bit planes + fp32 norms")
+DECODE_KERNEL = "decode_f4_kernel"
+DECODE_SOURCES = ["kv_cache_vector_19_b300/csrc/decode_f4.cuh", "kv_cache_vector_19_b300/csrc/dev_common.cuh"]
+TRAFFIC_PROFILE = "profiles/decode_f4_kernel_longctx.md"
+
+
+def source_fingerprint():
+    """sha256 (first 16 hex digits) of the decode kernel's sources, as recorded in profiles."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    kernel source being run (its 'source fingerprint:' line matches), else None."""
+    import re
+    try:
+        text = open(os.path.join(ROOT, TRAFFIC_PROFILE)).read()
+    except OSError:
+        return None
+    fp = re.search(r"source fingerprint:\s*([0-9a-f]{16})", text)
+    tb = re.search(r"traffic bytes per launch:\s*([0-9]+)", text)
+    if not fp or not tb or fp.group(1) != source_fingerprint():
+        return None
+    return int(tb.group(1))
 
 
 def bpt(d, b, m):
@@ -120,8 +153,10 @@ def job_gbs(world, bytes_per_rank, t_ms):
 
 def cpu_oracle_sample(w, seconds=12.0, reps_max=1000):
     """The oracle's own decode over packed pages (unpack + route A for the G query heads
-    of one KV head) on a 1024-token sample of the workload, repeated for ~`seconds`.
-    Returns (GB/s of compressed pages decoded, Mtokens/s quantized, threads, description)."""
+    of one KV head) on a 1024-token sample of the workload, repeated for ~`seconds` (half on
+    one thread, half with the BLAS pool).  Returns (GB/s of compressed pages decoded on one
+    thread, Mtokens/s quantized, threads of that figure (1), description, GB/s with the pool,
+    pool size)."""
     import numpy as np
 
     from oracle import decode as odec
@@ -145,26 +180,35 @@ def cpu_oracle_sample(w, seconds=12.0, reps_max=1000):
                                        ov["idx"][s], ov["n"][s]))
     cache = np.concatenate(pages)
     q = rng.standard_normal((G, d))
-    reps, t_dec = 0, 0.0
-    while t_dec < seconds and reps < reps_max:
-        t0 = time.perf_counter()
-        tok = pagefmt.unpack_tokens(d, b, m, cache, T // 128, 0, 0, T, 1)
-        tk = dict(idx=tok["kidx"], n=tok["nk"].astype(np.float64), sigma=tok["sigma"],
-                  gamma=tok["gamma"].astype(np.float64))
-        tv = dict(idx=tok["vidx"], n=tok["nv"].astype(np.float64))
-        for h in range(G):
-            odec.attend_route_a(q[h], tk, tv, p.Pi, p.S, p.cb_k, p.cb_v)
-        t_dec += time.perf_counter() - t0
-        reps += 1
-    gbs = reps * T * bpt(d, b, m) / t_dec / 1e9
+    def run(limit_s):
+        reps, t_dec = 0, 0.0
+        while t_dec < limit_s and reps < reps_max:
+            t0 = time.perf_counter()
+            tok = pagefmt.unpack_tokens(d, b, m, cache, T // 128, 0, 0, T, 1)
+            tk = dict(idx=tok["kidx"], n=tok["nk"].astype(np.float64), sigma=tok["sigma"],
+                      gamma=tok["gamma"].astype(np.float64))
+            tv = dict(idx=tok["vidx"], n=tok["nv"].astype(np.float64))
+            for h in range(G):
+                odec.attend_route_a(q[h], tk, tv, p.Pi, p.S, p.cb_k, p.cb_v)
+            t_dec += time.perf_counter() - t0
+            reps += 1
+        return reps * T * bpt(d, b, m) / t_dec / 1e9, reps, t_dec
+
     try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except ImportError:   # BLAS pools default to one thread per host core
-        threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count())))
-    desc = (f"oracle decode of 1 KV head x {T} tokens ({T // 128} packed pages) for {G} query heads, "
-            f"{reps} reps in {t_dec:.1f} s; oracle quantize of {T} K+V vectors in {t_quant:.2f} s")
-    return gbs, T / t_quant / 1e6, threads, desc
+        from threadpoolctl import threadpool_info, threadpool_limits
+        pool = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        with threadpool_limits(1):
+            gbs1, reps1, t1 = run(seconds / 2)
+    except ImportError:   # no pool control: the run below is the only figure
+        threadpool_limits, pool = None, 1
+    gbs, reps, t_dec = run(seconds / 2 if threadpool_limits else seconds)
+    if threadpool_limits is None:
+        gbs1, reps1, t1 = gbs, reps, t_dec
+    desc = (f"oracle decode of 1 KV head x {T} tokens ({T // 128} packed pages) for {G} query heads: "
+            f"{reps1} reps in {t1:.1f} s on 1 thread; {reps} reps in {t_dec:.1f} s with a {pool}-thread BLAS pool "
+            f"({gbs:.4f} GB/s; page unpacking is single-threaded Python either way); "
+            f"oracle quantize of {T} K+V vectors in {t_quant:.2f} s")
+    return gbs1, T / t_quant / 1e6, 1, desc, gbs, pool
 
 
 def run_reference(args, w):
@@ -176,7 +220,7 @@ def run_reference(args, w):
         cpu_oracle_sample(w, seconds=sample_s / 4, reps_max=1)
     vals, t_all = [], time.perf_counter()
     for _ in range(args.steps):
-        gbs, mtok, threads, desc = cpu_oracle_sample(w, seconds=sample_s)
+        gbs, mtok, threads, desc, _, _ = cpu_oracle_sample(w, seconds=sample_s)
         vals.append(gbs)
     elapsed = time.perf_counter() - t_all
     value = statistics.mean(vals)
@@ -355,7 +399,7 @@ def run_ours(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
         "data": "synthetic (seeded bf16 K/V, fp32 queries; no model weights)",
         "config": {"workload": f"{wl.name}: batch {B}, {H} KV / {Hq} query heads, head_dim {d}, b={wl.b}, "
                                f"{T} prefill tokens + {S} decode step(s)",
@@ -366,20 +410,24 @@ def run_ours(args, w):
         "quantize_ms": t_q,
         "decode_us_per_step": t_dphase / S * 1e3,
         "decode_call_us": t_call * 1e3,
-        "roofline": {"bound": "hbm", "kernel": "tq_attn_decode (decode_tc_kernel + prologue + combine)", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": f"tq_attn_decode ({DECODE_KERNEL} + prologue + combine)",
+                     "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": DECODE_TRAFFIC_BYTES, "algorithmic_bytes_per_launch": per_launch_bytes},
-        "e2e": {"value": job_gbs(world, dec_bytes, t_e2e_d), "unit": UNIT,
+                     "traffic": committed_traffic(), "traffic_source": TRAFFIC_PROFILE,
+                     "source_fingerprint": source_fingerprint(), "algorithmic_bytes_per_launch": per_launch_bytes},
+        "e2e": {"value": job_gbs(world, dec_bytes, t_e2e_q + t_e2e_d), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": t_e2e_q + t_e2e_d,
+                "note": "decode bytes over the whole step: prefill K/V copy + quantize, then 64 x (copies, append, decode, read-back)",
+                "decode_phase_gbs": job_gbs(world, dec_bytes, t_e2e_d),
                 "quantize_mtok_s": world * B * T / (t_e2e_q * 1e-3) / 1e6},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
     }
     if cpu is not None:
-        gbs, mtok, threads, desc = cpu
+        gbs, mtok, threads, desc, gbs_pool, pool = cpu
         line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
-                                "quantize_mtok_s": mtok}
+                                "quantize_mtok_s": mtok, "value_blas_pool": gbs_pool, "blas_pool_threads": pool}
     if rank == 0:
         print(json.dumps(line), flush=True)
     del g_dec, g_e2e

@@ -192,7 +192,9 @@ int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int q_heads, in
  * shared by every call on a device and keeps the last call's contents, so calls that can
  * overlap on the GPU (other streams, other threads) race: order them.  The first call on a
  * device looks up the scratch address (cudaGetSymbolAddress) and must come before any
- * stream capture.  Arguments and errors otherwise as tq_attn_decode. */
+ * stream capture.  A device reset (cudaDeviceReset) invalidates the looked-up address along with
+ * every context on that device; tq_ctx_create on the device makes the next call look it up
+ * again.  Arguments and error codes otherwise exactly as tq_attn_decode's. */
 int tq_attn_decode_noalloc(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
                            const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
                            float* logits_out, void* stream);

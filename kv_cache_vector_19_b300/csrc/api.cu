@@ -196,6 +196,8 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
     release(c);
     return rc;
   }
+  // a new context may follow a device reset, which invalidates the no-alloc scratch address
+  tq::noalloc_forget_device(device);
   *out = c;
   return TQ_OK;
 }
@@ -314,20 +316,32 @@ extern "C" size_t tq_decode_workspace_bytes(const tq_ctx* ctx, int batch, int q_
   return floats * sizeof(float);
 }
 
-extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
-                              const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
-                              float* logits_out, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!ctx || !q || !cache || !seq_lens || !out || !workspace) return TQ_EINVAL;
+namespace tq {
+// tq_attn_decode's checks of everything but the workspace: TQ_OK or the code it returns.
+int check_decode_args(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
+                      const int32_t* seq_lens, int max_tokens, const float* out, const float* logits_out) {
+  if (!ctx || !q || !cache || !seq_lens || !out) return TQ_EINVAL;
   if (batch < 1 || q_heads < 1 || kv_heads < 1 || max_tokens < 1) return TQ_EINVAL;
   if (batch > 65535 || kv_heads > 65535 || q_heads > 65535) return TQ_EINVAL;
   if (q_heads % kv_heads != 0) return TQ_EINVAL;
   if (q_heads / kv_heads > 16) return TQ_EUNSUPPORTED;
-  if (!aligned(q, 16) || !aligned(cache, 256) || !aligned(out, 16) || !aligned(workspace, 256) ||
-      !aligned(seq_lens, 4) || (logits_out && !aligned(logits_out, 4)))
+  if (!aligned(q, 16) || !aligned(cache, 256) || !aligned(out, 16) || !aligned(seq_lens, 4) ||
+      (logits_out && !aligned(logits_out, 4)))
     return TQ_EINVAL;
   tq::MmaPlan mp;
   const int kern = decode_kernel_for(ctx, batch, q_heads, kv_heads, max_tokens, &mp);
-  if (kern < 0) return kern;
+  return kern < 0 ? kern : TQ_OK;
+}
+}  // namespace tq
+
+extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                              const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
+                              float* logits_out, void* workspace, size_t workspace_bytes, void* stream) {
+  const int rc = tq::check_decode_args(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out);
+  if (rc != TQ_OK) return rc;
+  if (!workspace || !aligned(workspace, 256)) return TQ_EINVAL;
+  tq::MmaPlan mp;
+  const int kern = decode_kernel_for(ctx, batch, q_heads, kv_heads, max_tokens, &mp);
   if (workspace_bytes < tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens)) return TQ_ENOMEM;
   DeviceGuard guard(ctx->device);
   if (kern == TQ_DECODE_TC4)

@@ -78,11 +78,11 @@ constexpr int kWarpIS = 12;   // score-MMA issuer
 constexpr int kWarpIV0 = 13;  // value-MMA issuer, first half of the planes
 constexpr int kWarpIV1 = 14;  // value-MMA issuer, second half
 constexpr int kWarpWS = 15;   // score waiter
-constexpr int kWarpT2 = 16;   // token warps, second set
-constexpr int kWarpWV = 20;   // value waiter; page ring
-constexpr int kWarpsAll = 21;
-static_assert(kWarpT == 0, "the segment's n_ref is stored by thread 0 as the first token thread");
-constexpr int kL2Ahead = 12;
+constexpr int kWarpT2 = 16;   // token warps, further sets (16-19, 20-23, ...), then the value waiter
+constexpr int kTokenSets = 2; // token-warp sets (each a warp per TMEM lane quarter); at most GP
+constexpr int kL2Ahead = 12;  // pages prefetched into L2 beyond the shared-memory ring
+constexpr int kRingMax = 8;   // ring slots (as many as fit, at most this; a streaming probe
+                              // of this grid runs the whole cache through 4-8 slots at ~5 TB/s)
 // Lazy-maximum threshold (natural-log units): a page rescales the running maximum only when
 // one of its logits exceeds it by kTau or a value norm exceeds n_ref, so a weight
 // x = p n_v / n_ref stays below e^0.69 = 1.994 and Y = round(2^15 x) fits 16 bits.  The
@@ -93,7 +93,7 @@ constexpr float kWScale = 32768.f;
 constexpr int kNQP = 7;       // e2m1 pieces of a query operand
 constexpr int kNPW = 8;       // 2-bit pieces of a softmax weight (8 columns per head)
 constexpr int kSmemMax = 227 * 1024;
-constexpr int kNbVote0 = 1, kNbScore = 2, kNbValue = 3, kNbVote1 = 4;   // named barriers (vote: one per set)
+constexpr int kNbVote0 = 1, kNbScore = 2, kNbValue = 3, kNbVote1 = 4;   // named barriers (votes: 1, 4, 5, ..)
 
 __host__ __device__ constexpr int rnd(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -103,10 +103,13 @@ struct Cfg {
   using PL = PageLayout<128, BITS>;
   static constexpr int BK = BITS - 1, BV = BITS;
   static constexpr int PK = 1 << (BK - 1), PV = 1 << (BV - 1), NS = PK + 1;
-  static constexpr int TS = 2, HPT = GP / TS;          // token-warp sets, heads per set
-  static constexpr int THREADS = 32 * kWarpsAll;
+  static constexpr int TS = kTokenSets < GP ? kTokenSets : GP;   // token-warp sets
+  static constexpr int HPT = GP / TS;                  // query heads per token-warp set
+  static constexpr int WV = kWarpT2 + 4 * (TS - 1);    // value waiter; page ring
+  static constexpr int WARPS = WV + 1;
+  static constexpr int THREADS = 32 * WARPS;
   static constexpr int SCOLS = 8 * HPT;                // score columns of one term and set (8 per head)
-  static constexpr int NSC = 4 * SCOLS;                // [key: set 0 | set 1 | sign: set 0 | set 1]
+  static constexpr int NSC = 2 * TS * SCOLS;           // [key: set 0 | set 1 .. | sign: set 0 | set 1 ..]
   static constexpr int VCOLS = 8 * HPT;                // value columns (B_v rows) of one set, 8 per head
   static constexpr int NVC = TS * VCOLS;               // = 8 GP
   // tensor memory
@@ -132,18 +135,18 @@ struct Cfg {
   static constexpr int OFF_BV = OFF_BS + BS_BYTES;
   static constexpr int OFF_Q = OFF_BV + 2 * BV_BYTES;         // [GP][2][128] f32: q~, q_s
   static constexpr int OFF_HEAD = OFF_Q + GP * 2 * 128 * 4;   // [GP][4] f32
-  static constexpr int OFF_RED = OFF_HEAD + GP * 4 * 4;       // [8 token warps][HPT + 1] f32
-  static constexpr int OFF_F = OFF_RED + 8 * (HPT + 1) * 4;   // n_ref of each token-warp set
+  static constexpr int OFF_RED = OFF_HEAD + GP * 4 * 4;       // [4 TS token warps][HPT + 1] f32
+  static constexpr int OFF_F = OFF_RED + 4 * TS * (HPT + 1) * 4;   // n_ref of each token-warp set
   static constexpr int OFF_MBAR = rnd(OFF_F + 16, 8);
-  // full[8], empty[8], as_ready[2], as_free[2], s_fin[2], ds_free[2], av_ready[2], v_fin[2],
-  // bv_ready[2], teardown[3]
-  static constexpr int NMBAR = 16 + 14 + 3;
+  // full[kRingMax], empty[kRingMax], as_ready[2], as_free[2], s_fin[2], ds_free[2], av_ready[2],
+  // v_fin[2], bv_ready[2], teardown[3]
+  static constexpr int NMBAR = 2 * kRingMax + 14 + 3;
   static constexpr int OFF_MISC = OFF_MBAR + NMBAR * 8;       // tmem base, fail flag
   static constexpr int OFF_PAGES = rnd(OFF_MISC + 16, 128);
   static constexpr int NBUF_FIT = (kSmemMax - OFF_PAGES) / PAGE;
-  static constexpr int NBUF = NBUF_FIT > 8 ? 8 : NBUF_FIT;
+  static constexpr int NBUF = NBUF_FIT > kRingMax ? kRingMax : NBUF_FIT;
   static constexpr int SMEM = OFF_PAGES + NBUF * PAGE;
-  static constexpr bool SUPPORTED = TCOLS <= 512 && NBUF >= 4 && HPT % 2 == 0 && HPT >= 2 && kNPW <= 8;
+  static constexpr bool SUPPORTED = TCOLS <= 512 && NBUF >= 4 && HPT >= 1 && GP % TS == 0 && kNPW <= 8;
 };
 
 // OR-vote / barrier among the 128 threads of one token-warp set (named barrier id).
@@ -200,7 +203,8 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
   using PL = typename C::PL;
   constexpr int D = 128, NS = C::NS, PK = C::PK, PV = C::PV, BK = C::BK, BV = C::BV, NBUF = C::NBUF;
   constexpr int NSC = C::NSC, NVC = C::NVC, SCOLS = C::SCOLS, VCOLS = C::VCOLS, DSB = C::DSB;
-  constexpr int HPT = C::HPT, kThreads = C::THREADS, ASB = C::ASB, AVB = C::AVB;
+  constexpr int HPT = C::HPT, kThreads = C::THREADS, ASB = C::ASB, AVB = C::AVB, TS = C::TS;
+  constexpr int kWarpWV = C::WV, kWarpsAll = C::WARPS;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint8_t* s_pages = smem + C::OFF_PAGES;
   uint8_t* s_bs = smem + C::OFF_BS;
@@ -213,16 +217,16 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
   // Every hand-off barrier exists once per buffer (index = page & 1) and completes once per
   // page of that parity; every waiter has waited for the previous completion, so a parity wait
   // never mistakes an older phase for a newer one.
-  uint64_t* s_full = mb;            // [8]  page in ring slot landed (+ tx bytes)
-  uint64_t* s_empty = mb + 8;       // [8]  page read by the key- and value-plane warps (4 + 4)
-  uint64_t* as_ready = mb + 16;     // [2]  key planes of the page in A_s (4 warps)
-  uint64_t* as_free = mb + 18;      // [2]  score MMAs reading that A_s buffer done (commit)
-  uint64_t* s_fin = mb + 20;        // [2]  score MMAs into that D_s buffer done (commit)
-  uint64_t* ds_free = mb + 22;      // [2]  D_s buffer read by the token warps (8)
-  uint64_t* av_ready = mb + 24;     // [2]  value planes in that A_v buffer (4 warps)
-  uint64_t* v_fin = mb + 26;        // [2]  value MMAs of the page done (commits of 2 issuers)
-  uint64_t* bv_ready = mb + 28;     // [2]  B_v buffer written, D_v rescaled (8 token warps)
-  uint64_t* td_bar = mb + 30;       // [3]  teardown drains of the three issuers
+  uint64_t* s_full = mb;                 // [ring] page in ring slot landed (+ tx bytes)
+  uint64_t* s_empty = mb + kRingMax;     // [ring] page read by the key- and value-plane warps (4 + 4)
+  uint64_t* as_ready = mb + 2 * kRingMax;  // [2] key planes of the page in A_s (4 warps)
+  uint64_t* as_free = as_ready + 2;      // [2]  score MMAs reading that A_s buffer done (commit)
+  uint64_t* s_fin = as_ready + 4;        // [2]  score MMAs into that D_s buffer done (commit)
+  uint64_t* ds_free = as_ready + 6;      // [2]  D_s buffer read by the token warps (4 TS)
+  uint64_t* av_ready = as_ready + 8;     // [2]  value planes in that A_v buffer (4 warps)
+  uint64_t* v_fin = as_ready + 10;       // [2]  value MMAs of the page done (commits of 2 issuers)
+  uint64_t* bv_ready = as_ready + 12;    // [2]  B_v buffer written, D_v rescaled (4 TS token warps)
+  uint64_t* td_bar = as_ready + 14;      // [3]  teardown drains of the three issuers
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* s_fail = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
 
   if (warp == 0) tmem_alloc(s_tmem, 512);
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < NBUF; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 8);
     }
@@ -246,10 +250,10 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
       mbar_init(&as_ready[i], 4);
       mbar_init(&as_free[i], 1);
       mbar_init(&s_fin[i], 1);
-      mbar_init(&ds_free[i], 8);
+      mbar_init(&ds_free[i], 4 * TS);
       mbar_init(&av_ready[i], 4);
       mbar_init(&v_fin[i], 2);
-      mbar_init(&bv_ready[i], 8);
+      mbar_init(&bv_ready[i], 4 * TS);
     }
     for (int i = 0; i < 3; ++i) mbar_init(&td_bar[i], 1);
     *s_fail = 0;
@@ -272,7 +276,8 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
   __syncthreads();
   tc_fence_after();
 
-  constexpr uint32_t idesc_s = make_idesc_mxf4(128, NSC);
+  // key-plane MMAs write the key half of the score columns, sign-plane MMAs the sign half
+  constexpr uint32_t idesc_s = make_idesc_mxf4(128, NSC / 2);
   constexpr uint32_t idesc_v = make_idesc_mxf4(128, NVC);
   const uint32_t sfa = tmem + C::TSF, sfb = tmem + C::TSF + 4;
 
@@ -363,8 +368,8 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
     for (int e = tid; e < NSC * NS * 16; e += kThreads) {
       const int n = e / (NS * 16), w = e % (NS * 16);
       const int pl = w / 16, c = (w % 16) / 4, s = w % 4;
-      const bool sign_term = n >= 2 * SCOLS;
-      const int set = (n % (2 * SCOLS)) / SCOLS, lc = n % SCOLS;
+      const bool sign_term = n >= TS * SCOLS;
+      const int set = (n % (TS * SCOLS)) / SCOLS, lc = n % SCOLS;
       const int hh = set * HPT + lc / 8, piece = lc % 8;
       uint32_t word = 0u;
       if (piece < kNQP && hh < G && (sign_term ? pl == PK : pl < PK)) {
@@ -401,8 +406,10 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
         // ============ score MMAs: D_s[token][column] = A_s[token][planes] x B_s ============
         uint64_t bd[NS * 2];
         const uint32_t bs = smem_u32(s_bs);
+        constexpr uint32_t SBO = C::BS_ROWB / 16 * 128;   // bytes per 8-row group of B_s
 #pragma unroll
-        for (int ks = 0; ks < NS * 2; ++ks) bd[ks] = smem_desc(bs + ks * 256, 128, C::BS_ROWB / 16 * 128);
+        for (int ks = 0; ks < NS * 2; ++ks)   // the sign half starts at row NSC / 2
+          bd[ks] = smem_desc(bs + (ks >= 2 * PK ? (NSC / 2 / 8) * SBO : 0u) + ks * 256, 128, SBO);
         for (int p = 0; p < n_pages; ++p) {
           const uint32_t g = pg_base + p, x = g & 1;
           const uint32_t d = tmem + C::TD_S + (DSB == 2 ? x : 0) * NSC;
@@ -411,7 +418,8 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
           if (lane == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < NS * 2; ++ks) mma_f4_ts(d, as + 8 * ks, bd[ks], idesc_s, sfa, sfb, ks > 0);
+            for (int ks = 0; ks < NS * 2; ++ks)
+              mma_f4_ts(d + (ks >= 2 * PK ? NSC / 2 : 0), as + 8 * ks, bd[ks], idesc_s, sfa, sfb, ks != 0 && ks != 2 * PK);
             tc_commit(&as_free[x]);
             tc_commit(&s_fin[x]);
           }
@@ -549,10 +557,10 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
           __syncwarp();
           if (lane == 0) mbar_arrive(&av_ready[x]);
         }
-      } else if ((warp >= kWarpT && warp < kWarpT + 4) || (warp >= kWarpT2 && warp < kWarpT2 + 4)) {
+      } else if ((warp >= kWarpT && warp < kWarpT + 4) || (warp >= kWarpT2 && warp < kWarpWV)) {
         // ============ token warps: logits, lazy softmax, weight pieces -> B_v ============
         // set ts handles heads h0 .. h0 + HPT - 1: their D_s columns, D_v columns and B_v rows
-        const int twarp = warp >= kWarpT2 ? 4 + (warp - kWarpT2) : warp - kWarpT;   // 0 .. 7
+        const int twarp = warp >= kWarpT2 ? 4 + (warp - kWarpT2) : warp - kWarpT;   // 0 .. 4 TS - 1
         const int ts = twarp >> 2, h0 = ts * HPT, q4 = warp & 3;
         const int tau = slot_of_lane(row);
         float m_run[HPT], l_part[HPT];
@@ -562,7 +570,7 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
           l_part[h] = 0.f;
         }
         float n_ref = 0.f;
-        const int vote_id = ts == 0 ? kNbVote0 : kNbVote1;
+        const int vote_id = ts == 0 ? kNbVote0 : kNbVote1 + ts - 1;
         for (int p = 0; p < n_pages; ++p) {
           const uint32_t g = pg_base + p, x = g & 1;
           const uint32_t db = DSB == 2 ? x : 0;
@@ -584,22 +592,23 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
           int ovf = nvt > n_ref;
           {
             const uint32_t base = tl + C::TD_S + db * NSC + ts * SCOLS;
+            constexpr int HR = HPT < 2 ? HPT : 2;   // heads per round of loads
 #pragma unroll
-            for (int h2 = 0; h2 < HPT; h2 += 2) {
-              uint32_t rk[2][8], rq[2][8];
+            for (int h2 = 0; h2 < HPT; h2 += HR) {
+              uint32_t rk[HR][8], rq[HR][8];
 #pragma unroll
-              for (int u = 0; u < 2; ++u) {
+              for (int u = 0; u < HR; ++u) {
                 tmem_ld8(base + 8 * (h2 + u), rk[u]);
-                tmem_ld8(base + 2 * SCOLS + 8 * (h2 + u), rq[u]);
+                tmem_ld8(base + TS * SCOLS + 8 * (h2 + u), rq[u]);
               }
               tc_wait_ld();
-              if (h2 + 2 >= HPT) {
+              if (h2 + HR >= HPT) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ds_free[x]);
               }
 #pragma unroll
-              for (int u = 0; u < 2; ++u) {
+              for (int u = 0; u < HR; ++u) {
                 const int h = h2 + u, hg = h0 + h;
                 const float2 hc = *reinterpret_cast<const float2*>(s_head + hg * 4 + 2);
                 float sk = __uint_as_float(rk[u][kNQP - 1]), sq = __uint_as_float(rq[u][kNQP - 1]);

@@ -27,7 +27,8 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_decode_scratch on `device` (which must be current), looked up once.
+// Device address of g_decode_scratch on `device` (which must be current), looked up once per
+// device and again after tq_ctx_create on that device (a device reset reloads the module).
 int scratch_address(int device, void** out) {
   if (device < 0 || device >= kMaxDevices) return TQ_EINVAL;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -42,10 +43,20 @@ int scratch_address(int device, void** out) {
 
 }  // namespace
 
+namespace tq {
+void noalloc_forget_device(int device) {
+  if (device < 0 || device >= kMaxDevices) return;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_scratch_addr[device] = nullptr;
+}
+}  // namespace tq
+
 extern "C" int tq_attn_decode_noalloc(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
                                       const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
                                       float* logits_out, void* stream) {
-  if (!ctx) return TQ_EINVAL;
+  // the same checks and error codes as tq_attn_decode, then the scratch size
+  const int chk = tq::check_decode_args(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out);
+  if (chk != TQ_OK) return chk;
   const size_t need = tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens);
   if (need == 0) return TQ_EINVAL;
   if (need > kScratchBytes) return TQ_ESCRATCH;

@@ -113,6 +113,12 @@ int prepare_decode_f4(const tq_ctx* c);
 int launch_decode_f4(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                      const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
                      void* workspace, void* stream);
+// tq_attn_decode's argument checks except the workspace (TQ_OK or its error code).
+int check_decode_args(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
+                      const int32_t* seq_lens, int max_tokens, const float* out, const float* logits_out);
+// Drops the no-alloc entry point's cached scratch address of a device (looked up again on the
+// next call there).
+void noalloc_forget_device(int device);
 // q~ = Pi q and q_s = S q for every (batch, query head), fp32.
 void launch_prologue(const tq_ctx* c, const float* q, int batch, int q_heads, float* qr, float* qs,
                      cudaStream_t st);

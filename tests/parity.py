@@ -19,11 +19,10 @@ from oracle import pagefmt, params, quant
 MISMATCH_RATE = 1e-4
 LOGIT_ATOL = 2e-3
 OUT_REL_L2 = 1e-2
-# Decode against the oracle on the GPU's own pages (no quantizer flips): the tensor-core
-# path carries each softmax weight in two e4m3 pieces (hi + lo/16, relative error at most
-# 2^-8 = 3.9e-3 per weight, typically ~1e-3), so the output differs from the exact weighted
-# sum by about that much relative to the output norm.
-OUT_ON_PAGES_REL_L2 = 5e-3
+# Decode against the oracle on the GPU's own pages (no quantizer flips): only the decode
+# arithmetic differs, and it is held to the same 2e-3 that the acceptance statement gives the
+# attention scores, here as the relative L2 error of each output row.
+OUT_ON_PAGES_REL_L2 = 2e-3
 
 
 class Run:

@@ -81,7 +81,7 @@ def _check_decode(d, b, G, path="auto"):
 
 
 @pytest.mark.parametrize("d,b,G", [(64, 2, 1), (128, 3, 4), (128, 4, 8), (256, 5, 16), (256, 3, 2),
-                                   (64, 5, 16), (128, 2, 3)])
+                                   (64, 5, 16), (128, 2, 3), (64, 3, 4), (64, 4, 4), (256, 2, 4)])
 def test_decode_small(d, b, G):
     _check_decode(d, b, G)
 
@@ -110,12 +110,13 @@ def test_decode_path_selection():
         assert ctx.workspace_bytes(2, 8, 2, 700) > 0
 
 
-@pytest.mark.parametrize("path", ["tc4", "tc", "mma", "simt"])
-def test_decode_long_sequences_each_kernel(path):
+@pytest.mark.parametrize("path,d,b", [("tc4", 128, 3), ("tc", 128, 3), ("mma", 128, 3), ("simt", 128, 3),
+                                      ("auto", 64, 3), ("auto", 256, 2)])
+def test_decode_long_sequences_each_kernel(path, d, b):
     """Sequences of ~120 pages, so that every CTA of the bit-plane kernels streams far more
     pages than its shared-memory ring holds (ring refills, many segments), checked on two
     heads against the oracle on the GPU's own pages."""
-    d, b, G, B, H, maxT = 128, 3, 4, 2, 8, 15360
+    G, B, H, maxT = 4, 2, 8, 15360
     run = P.Run(d, b, B, H, G * H, maxT, decode_path=path)
     gen = torch.Generator().manual_seed(11)
     for bb in range(B):   # quantize one sequence at a time to keep host memory small

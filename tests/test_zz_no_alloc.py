@@ -62,3 +62,27 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
                                         _ptr(dummy), None, _stream())
     assert rc == tq.TQ_ESCRATCH
     ctx.close()
+
+
+def test_noalloc_returns_the_same_errors_as_decode():
+    """A call the forced kernel cannot serve (the e2m1 tcgen05 kernel takes at most 8 query
+    heads per KV head; here 12) and a group size that does not divide give tq_attn_decode's own
+    error codes, not a generic one."""
+    B, H, T, d = 1, 2, 256, 128
+    ctx = tq.Context(d, 3, seed=0)
+    ctx.set_decode_path("tc4")
+    cache = ctx.alloc_cache(B, H, T)
+    q = torch.zeros(B, 24, d, device="cuda")
+    out = torch.empty_like(q)
+    lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    rc_ref = binding.tq_attn_decode(ctx.handle, _ptr(q), B, 24, H, _ptr(cache), _ptr(lens), T, _ptr(out), None,
+                                    _ptr(ws), ws.numel(), _stream())
+    rc = binding.tq_attn_decode_noalloc(ctx.handle, _ptr(q), B, 24, H, _ptr(cache), _ptr(lens), T, _ptr(out), None,
+                                        _stream())
+    assert rc == rc_ref == tq.TQ_EUNSUPPORTED
+    q3 = torch.zeros(B, 6, d, device="cuda")          # 6 query heads over 4 KV heads
+    rc = binding.tq_attn_decode_noalloc(ctx.handle, _ptr(q3), B, 6, 4, _ptr(cache), _ptr(lens), T, _ptr(q3), None,
+                                        _stream())
+    assert rc == tq.TQ_EINVAL
+    ctx.close()
