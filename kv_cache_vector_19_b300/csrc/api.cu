@@ -7,7 +7,10 @@
 #include <new>
 #include <vector>
 
+#include <cuda_fp16.h>
+
 #include "bitplane.h"
+#include "exact.cuh"
 #include "tq_internal.h"
 
 namespace {
@@ -45,24 +48,15 @@ std::vector<double> plane_alphas(const std::vector<double>& book, int bits) {
   return al;
 }
 
-uint16_t bf16_rne(float x) {   // round to nearest even (finite inputs)
-  uint32_t u;
-  std::memcpy(&u, &x, 4);
-  u += 0x7FFFu + ((u >> 16) & 1u);
-  return (uint16_t)(u >> 16);
-}
-float bf16_to_f(uint16_t h) {
-  uint32_t u = (uint32_t)h << 16;
-  float f;
-  std::memcpy(&f, &u, 4);
-  return f;
-}
+uint16_t f16_bits(double x) { return __half_as_ushort(__float2half_rn((float)x)); }
+double f16_val(uint16_t h) { return (double)__half2float(__ushort_as_half(h)); }
 
-// bf16 hi/lo operand blob of the tensor-core quantizer (head_dim 128): matrices M[n][k]
-// (Pi, then S' = S Pi^T) split as hi = bf16(M), lo = bf16(M - hi), each stored in the
-// no-swizzle K-major layout (8-row x 16-byte core matrices, 128 contiguous bytes each;
-// core (n/8, k/8) at (n/8) * 2048 + (k/8) * 128).
-std::vector<uint8_t> quantizer_blob(const std::vector<double>& pi, const std::vector<double>& spt_kmajor) {
+// fp16 hi/lo operand blob of the tensor-core quantizer (head_dim 128): matrices M[n][k]
+// (Pi, then S' = S Pi^T), scaled by 2^8 so that the lo pieces stay clear of fp16's subnormal
+// range, split as hi = f16(256 M), lo = f16(256 M - hi), each stored in the no-swizzle K-major
+// layout (8-row x 16-byte core matrices, 128 contiguous bytes each; core (n/8, k/8) at
+// (n/8) * 2048 + (k/8) * 128).
+std::vector<uint8_t> quantizer_blob(const std::vector<double>& pi, const std::vector<double>& sp) {
   const int d = 128;
   std::vector<uint8_t> blob(4 * d * d * 2);
   auto put = [&](int mat, int n, int k, uint16_t v) {
@@ -72,15 +66,39 @@ std::vector<uint8_t> quantizer_blob(const std::vector<double>& pi, const std::ve
   };
   for (int n = 0; n < d; ++n)
     for (int k = 0; k < d; ++k) {
-      const float p = (float)pi[(size_t)n * d + k];   // rotation: y_n = sum_k Pi[n][k] x_k
-      const float s = (float)spt_kmajor[(size_t)n * d + k];   // projection: z_n = sum_k S'[n][k] r_k
-      const uint16_t ph = bf16_rne(p), sh = bf16_rne(s);
+      const double p = 256.0 * pi[(size_t)n * d + k];   // rotation: y_n = sum_k Pi[n][k] x_k
+      const double s = 256.0 * sp[(size_t)n * d + k];   // projection: z_n = sum_k S'[n][k] r_k
+      const uint16_t ph = f16_bits(p), sh = f16_bits(s);
       put(0, n, k, ph);
-      put(1, n, k, bf16_rne(p - bf16_to_f(ph)));
+      put(1, n, k, f16_bits(p - f16_val(ph)));
       put(2, n, k, sh);
-      put(3, n, k, bf16_rne(s - bf16_to_f(sh)));
+      put(3, n, k, f16_bits(s - f16_val(sh)));
     }
   return blob;
+}
+
+// Host image of the exact-decision tables (layout of tq::exact::tables).
+std::vector<float> exact_tables(const tq_ctx* c, const std::vector<double>& sp) {
+  const int d = c->d;
+  const size_t dd = (size_t)d * d;
+  std::vector<float> t(tq::exact::tables_floats(d), 0.f);
+  auto split = [&](const double* src, size_t n, size_t off_hi, size_t off_lo) {
+    for (size_t i = 0; i < n; ++i) {
+      const float hi = (float)src[i];
+      t[off_hi + i] = hi;
+      t[off_lo + i] = (float)(src[i] - (double)hi);
+    }
+  };
+  split(c->pi.data(), dd, 0, dd);
+  split(c->s.data(), dd, 2 * dd, 3 * dd);
+  split(sp.data(), dd, 4 * dd, 5 * dd);
+  const size_t b = 6 * dd;
+  split(c->tk.data(), c->tk.size(), b, b + 32);
+  split(c->tv.data(), c->tv.size(), b + 64, b + 96);
+  split(c->ck.data(), c->ck.size(), b + 128, b + 160);
+  tq::exact::near_table(c->tk.data(), c->lk, &t[b + 192]);
+  tq::exact::near_table(c->tv.data(), c->lv, &t[b + 256]);
+  return t;
 }
 
 void release(tq_ctx* c) {
@@ -89,7 +107,7 @@ void release(tq_ctx* c) {
   cudaGetDevice(&prev);
   cudaSetDevice(c->device);
   float* bufs[] = {c->d_pi, c->d_pit, c->d_st, c->d_spt, c->d_s, c->d_ck, c->d_tk, c->d_cv, c->d_tv,
-                   c->d_alpha_k, c->d_alpha_v};
+                   c->d_alpha_k, c->d_alpha_v, c->d_exact};
   for (float* p : bufs)
     if (p) cudaFree(p);
   if (c->d_status) cudaFree(c->d_status);
@@ -176,10 +194,16 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
     if (rc == TQ_OK) rc = tq::prepare_decode_mma(c);
     if (rc == TQ_OK) rc = tq::prepare_decode_tc(c);
     if (rc == TQ_OK) rc = tq::prepare_decode_f4(c);
+    std::vector<double> sp((size_t)m * d);   // S'[i][j] row-major
+    for (int i = 0; i < m; ++i)
+      for (int j = 0; j < d; ++j) sp[(size_t)i * d + j] = spt[(size_t)j * m + i];
+    if (rc == TQ_OK) {
+      const std::vector<float> et = exact_tables(c, sp);
+      if (cudaMalloc(reinterpret_cast<void**>(&c->d_exact), et.size() * sizeof(float)) != cudaSuccess ||
+          cudaMemcpy(c->d_exact, et.data(), et.size() * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess)
+        rc = TQ_ENOMEM;
+    }
     if (rc == TQ_OK && d == 128) {
-      std::vector<double> sp((size_t)m * d);   // S'[i][j] row-major
-      for (int i = 0; i < m; ++i)
-        for (int j = 0; j < d; ++j) sp[(size_t)i * d + j] = spt[(size_t)j * m + i];
       std::vector<uint8_t> blob = quantizer_blob(c->pi, sp);
       if (cudaMalloc(reinterpret_cast<void**>(&c->d_qblob), blob.size()) != cudaSuccess ||
           cudaMemcpy(c->d_qblob, blob.data(), blob.size(), cudaMemcpyHostToDevice) != cudaSuccess)

@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "exact.cuh"
 #include "layout.cuh"
 #include "tq_internal.h"
 
@@ -42,7 +43,7 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
                                                          const float* __restrict__ pit, const float* __restrict__ spt,
                                                          const float* __restrict__ ck, const float* __restrict__ tk,
                                                          const float* __restrict__ cv, const float* __restrict__ tv,
-                                                         int* status) {
+                                                         const float* __restrict__ exact_tabs, int* status) {
   using PL = PageLayout<D, BITS>;
   constexpr int M = D, BK = BITS - 1, BV = BITS, LK = 1 << BK, LV = 1 << BV;
   constexpr int NT = 4 * D, KQ = D / 4;   // 4 D threads: coordinate j, quarter qp of each sum
@@ -50,6 +51,7 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
   __shared__ float s_pa[4][D], s_pb[4][D];   // partial sums of the quarters
   __shared__ float s_red[NT / 32];
   __shared__ uint32_t s_words[BK * PL::KW + PL::SW];   // the slot's key-code and sign words
+  __shared__ int s_code[D];                            // the key's codes (exact sign decisions)
   const int j = threadIdx.x % D, qp = threadIdx.x / D;
   const int t = blockIdx.x, seq = blockIdx.y, b = seq / kv_heads;
   const int start = start_pos[b];
@@ -94,8 +96,43 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
   for (int q = 0; q < LK - 1; ++q) idx += uk >= tk[q] ? 1 : 0;
 #pragma unroll
   for (int q = 0; q < LV - 1; ++q) vidx += uv >= tv[q] ? 1 : 0;
+  // codes next to a boundary are taken again exactly (exact.cuh), each warp for its own 32
+  // coordinates (the warps of the four quarters repeat the same decisions)
+  const exact::Tables T = exact::tables(exact_tabs, D);
+  const int lane = threadIdx.x & 31;
+  {
+    const bool nk_near = nk > 0.f && fabsf(uk - T.nkt[2 * idx]) > T.nkt[2 * idx + 1];
+    const bool nv_near = nv > 0.f && fabsf(uv - T.nvt[2 * vidx]) > T.nvt[2 * vidx + 1];
+    uint32_t ev = __ballot_sync(0xffffffffu, nk_near);
+    if (ev) {
+      float x[D / 32];
+      exact::load_row<D>(k + row, lane, x);
+      const exact::F2 n = exact::norm<D>(x);
+      while (ev) {
+        const int L = __ffs(ev) - 1;
+        ev &= ev - 1;
+        const int r2 = exact::code<D>(x, n, T.pih, T.pil, __shfl_sync(0xffffffffu, j, L), T.tkh, T.tkl, LK - 1, lane);
+        if (lane == L) idx = r2;
+      }
+    }
+    ev = __ballot_sync(0xffffffffu, nv_near);
+    if (ev) {
+      float x[D / 32];
+      exact::load_row<D>(v + row, lane, x);
+      const exact::F2 n = exact::norm<D>(x);
+      while (ev) {
+        const int L = __ffs(ev) - 1;
+        ev &= ev - 1;
+        const int r2 = exact::code<D>(x, n, T.pih, T.pil, __shfl_sync(0xffffffffu, j, L), T.tvh, T.tvl, LV - 1, lane);
+        if (lane == L) vidx = r2;
+      }
+    }
+  }
   const float r = yk - nk * ck[idx];   // residual in the rotated frame
-  if (qp == 0) s_r[j] = r;
+  if (qp == 0) {
+    s_r[j] = r;
+    s_code[j] = idx;
+  }
   const float gamma = sqrtf(block_sum<NT>(qp == 0 ? r * r : 0.f, s_red));
   // z_i = (S' Pi r)_i = sum_c S'^T[c][i] (Pi r)_c; thread (j, qp) sums quarter qp for z_j (m == d)
   {
@@ -111,13 +148,33 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
   __syncthreads();
   const float z = (s_pa[0][j] + s_pa[1][j]) + (s_pa[2][j] + s_pa[3][j]);
   if (qp != 0) return;   // the rest is per coordinate
+  // projections next to zero: exact sign
+  bool sgn = z >= 0.f;
+  {
+    uint32_t ev = __ballot_sync(0xffffffffu, fabsf(z) < exact::kDeltaSign * gamma);
+    if (ev) {
+      float x[D / 32];
+      int codes[D / 32];
+      exact::load_row<D>(k + row, lane, x);
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) codes[q] = s_code[lane * (D / 32) + q];
+      const exact::F2 n = exact::norm<D>(x);
+      while (ev) {
+        const int L = __ffs(ev) - 1;
+        ev &= ev - 1;
+        const bool e2 = exact::sign<D>(x, n, codes, T.sh, T.sl, T.qh, T.ql, T.ckh, T.ckl,
+                                       __shfl_sync(0xffffffffu, j, L), lane);
+        if (lane == L) sgn = e2;
+      }
+    }
+  }
   // the slot's words: coordinate j of each key-code plane and of the sign plane
   int w, bit;
   coord_pos<D>(j, w, bit);
 #pragma unroll
   for (int q = 0; q < BK; ++q)
     if ((idx >> q) & 1) atomicOr(&s_words[q * PL::KW + w], 1u << bit);
-  if (z >= 0.f) atomicOr(&s_words[BK * PL::KW + w], 1u << bit);
+  if (sgn) atomicOr(&s_words[BK * PL::KW + w], 1u << bit);
   asm volatile("bar.sync 1, %0;" ::"r"(D) : "memory");   // the D remaining threads (warps 0 .. D/32-1)
   uint32_t* kc = reinterpret_cast<uint32_t*>(pg + PL::off_kcodes);
   uint32_t* sg = reinterpret_cast<uint32_t*>(pg + PL::off_signs);
@@ -147,7 +204,7 @@ int launch_one(const tq_ctx* c, const void* k, const void* v, int batch, int kv_
   quantize_few_kernel<D, BITS><<<grid, 4 * D, 0, st>>>(
       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), kv_heads, n_tokens, max_tokens,
       (max_tokens + 127) / 128, start_pos, static_cast<uint8_t*>(cache), c->d_pit, c->d_spt, c->d_ck, c->d_tk,
-      c->d_cv, c->d_tv, c->d_status);
+      c->d_cv, c->d_tv, c->d_exact, c->d_status);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
 }
 

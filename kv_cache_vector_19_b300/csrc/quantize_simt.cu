@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "exact.cuh"
 #include "layout.cuh"
 #include "tq_internal.h"
 
@@ -35,6 +36,7 @@ struct QArgs {
   const float* tk;
   const float* cv;
   const float* tv;
+  const float* exact;   // exact-decision tables
   int* status;
 };
 
@@ -124,6 +126,26 @@ __device__ __forceinline__ int encode(float yhat, const float* t) {
   return idx;
 }
 
+// Warp-collective: the codes of this warp's coordinates that the fast value put next to a
+// boundary, taken again exactly (exact.cuh); returns this thread's (possibly new) code.
+template <int D>
+__device__ __forceinline__ int resolve_codes(bool near, int idx, int row, int j, const __nv_bfloat16* src_seq,
+                                             int page, int start, int s0, const float* th, const float* tl, int nb,
+                                             const exact::Tables& T, int lane) {
+  uint32_t ev = __ballot_sync(0xffffffffu, near);
+  while (ev) {
+    const int L = __ffs(ev) - 1;
+    ev &= ev - 1;
+    const int rowL = __shfl_sync(0xffffffffu, row, L), jL = __shfl_sync(0xffffffffu, j, L);
+    float x[D / 32];
+    exact::load_row<D>(src_seq + ((long)page * 128 + s0 + rowL - start) * D, lane, x);
+    const exact::F2 n = exact::norm<D>(x);
+    const int r = exact::code<D>(x, n, T.pih, T.pil, jL, th, tl, nb, lane);
+    if (lane == L) idx = r;
+  }
+  return idx;
+}
+
 template <int D, int BITS>
 __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
   using PL = PageLayout<D, BITS>;
@@ -137,7 +159,9 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
   float* s_tk = s_ck + LK;
   float* s_cv = s_tk + LK;
   float* s_tv = s_cv + LV;
-  uint8_t* kcode = reinterpret_cast<uint8_t*>(s_tv + LV);          // [64][D]
+  float2* s_nk = reinterpret_cast<float2*>(s_tv + LV);              // near tables, one float2 per cell
+  float2* s_nv = s_nk + LK;
+  uint8_t* kcode = reinterpret_cast<uint8_t*>(s_nv + LV);          // [64][D]
   uint8_t* vcode = kcode + kRows * D;                              // [128][D]
 
   const int tid = threadIdx.x;
@@ -156,6 +180,10 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
   for (int i = tid; i < LK - 1; i += kThreads) s_tk[i] = a.tk[i];
   for (int i = tid; i < LV; i += kThreads) s_cv[i] = a.cv[i];
   for (int i = tid; i < LV - 1; i += kThreads) s_tv[i] = a.tv[i];
+  const exact::Tables T = exact::tables(a.exact, D);
+  for (int i = tid; i < 2 * LK; i += kThreads) reinterpret_cast<float*>(s_nk)[i] = T.nkt[i];
+  for (int i = tid; i < 2 * LV; i += kThreads) reinterpret_cast<float*>(s_nv)[i] = T.nvt[i];
+  const int lane = tid & 31;
 
   const size_t seq = (size_t)b * a.kv_heads + h;
   uint8_t* pg = a.cache + (seq * a.pages_per_seq + page) * (size_t)PL::bytes;
@@ -182,6 +210,8 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
       float y = ys[row * (D + 1) + j];
       float yh = n > 0.f ? y / n : 0.f;
       int idx = encode<LK>(yh, s_tk);
+      const bool near = n > 0.f && fabsf(yh - s_nk[idx].x) > s_nk[idx].y;
+      idx = resolve_codes<D>(near, idx, row, j, kseq, page, start, s0, T.tkh, T.tkl, LK - 1, T, lane);
       kcode[row * D + j] = (uint8_t)idx;
       ys[row * (D + 1) + j] = y - n * s_ck[idx];                   // r_rot = Pi r
     }
@@ -200,6 +230,27 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
       }
     }
     gemm64<D, D>(ys, a.spt, xs);                                     // Z = R S'^T
+    __syncthreads();
+    // projections next to zero: exact sign (stored back into Z as +-1)
+    for (int e = tid; e < kRows * D; e += kThreads) {
+      const int row = e / D, i = e % D;
+      const float z = xs[row * (D + 1) + i];
+      const bool near = fabsf(z) < exact::kDeltaSign * gam[row];
+      uint32_t ev = __ballot_sync(0xffffffffu, near);
+      while (ev) {
+        const int L = __ffs(ev) - 1;
+        ev &= ev - 1;
+        const int rowL = __shfl_sync(0xffffffffu, row, L), iL = __shfl_sync(0xffffffffu, i, L);
+        float x[D / 32];
+        int codes[D / 32];
+        exact::load_row<D>(kseq + ((long)page * 128 + s0 + rowL - start) * D, lane, x);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) codes[q] = kcode[rowL * D + lane * (D / 32) + q];
+        const exact::F2 n = exact::norm<D>(x);
+        const bool sg = exact::sign<D>(x, n, codes, T.sh, T.sl, T.qh, T.ql, T.ckh, T.ckl, iL, lane);
+        if (lane == L) xs[row * (D + 1) + i] = sg ? 1.f : -1.f;
+      }
+    }
     __syncthreads();
     // bit-pack key codes (BK planes) and signs, one word per thread-iteration
     constexpr int WPR = D / 32;
@@ -237,7 +288,10 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
       int row = e / D, j = e % D;
       float n = nrm[row];
       float yh = n > 0.f ? ys[row * (D + 1) + j] / n : 0.f;
-      vcode[(s0 + row) * D + j] = (uint8_t)encode<LV>(yh, s_tv);
+      int idx = encode<LV>(yh, s_tv);
+      const bool near = n > 0.f && fabsf(yh - s_nv[idx].x) > s_nv[idx].y;
+      idx = resolve_codes<D>(near, idx, row, j, vseq, page, start, s0, T.tvh, T.tvl, LV - 1, T, lane);
+      vcode[(s0 + row) * D + j] = (uint8_t)idx;
     }
     for (int row = tid; row < kRows; row += kThreads) {
       int slot = s0 + row;
@@ -269,7 +323,7 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
 
 template <int D>
 constexpr size_t quant_smem_bytes() {
-  return (size_t)2 * kRows * (D + 1) * 4 + 2 * kRows * 4 + (32 + 32 + 32 + 32) * 4 + (size_t)kRows * D +
+  return (size_t)2 * kRows * (D + 1) * 4 + 2 * kRows * 4 + (32 + 32 + 32 + 32 + 64 + 64) * 4 + (size_t)kRows * D +
          (size_t)128 * D;
 }
 
@@ -300,6 +354,7 @@ int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_he
   a.tk = c->d_tk;
   a.cv = c->d_cv;
   a.tv = c->d_tv;
+  a.exact = c->d_exact;
   a.status = c->d_status;
   dim3 grid((n_tokens + 127) / 128 + 1, kv_heads, batch);
   quantize_simt_kernel<D, BITS><<<grid, kThreads, smem, st>>>(a);

@@ -1,4 +1,4 @@
-// tq_quantize_kv on 5th-generation tensor cores (tcgen05, kind::f16, bf16), head_dim 128.
+// tq_quantize_kv on 5th-generation tensor cores (tcgen05, kind::f16, fp16 pieces), head_dim 128.
 //
 // [BLOG] "Технология TurboQuant и её применение с локальными LLM", section 1.2: every key
 // and value vector is rotated by the random orthogonal Pi and each rotated coordinate of
@@ -7,14 +7,17 @@
 // The residual is projected in the rotated frame: S r = S' (Pi r) with S' = S Pi^T and
 // Pi r = y - n c[idx].
 //
-// The three d x d contractions run on tcgen05 with fp32 accumulators in tensor memory.  K
-// and V are exact in bf16; Pi, S' and the rotated residual are split into bf16 hi + lo:
+// The three d x d contractions run on tcgen05 with fp32 accumulators in tensor memory.  Every
+// K / V row is scaled by a power of two (its largest magnitude into [2^14, 2^15)) and is then
+// exact in fp16; 256 Pi, 256 S' and the scaled rotated residual are split into fp16 hi + lo:
 //   Y   = X Pi_hi^T + X Pi_lo^T                       (keys and values, 2 x 8 MMAs each)
 //   Z   = R_hi S'_hi^T + R_hi S'_lo^T + R_lo S'_hi^T   (keys, 3 x 8 MMAs, R in tensor memory)
-// which keeps the rotation within ~2^-17 relative, far below what moves a code or a sign
-// except at a quantizer boundary.
+// which keeps the rotation within ~2^-20 of ||x||.  A code whose yhat lands within 2^-18 of a
+// boundary, or a sign whose projection lands within 2^-14 ||r|| of zero, is taken again in
+// double-float arithmetic (exact.cuh) by the warp that owns the row, so the page holds the
+// decisions of exact arithmetic.
 //
-// Persistent CTAs (one per SM): the bf16 operand blob (Pi hi/lo, S' hi/lo, 128 KB) is
+// Persistent CTAs (one per SM): the fp16 operand blob (Pi hi/lo, S' hi/lo, 128 KB) is
 // copied into shared memory once; every work item is the slots of one page that the call
 // writes, for one (batch, KV head).  Per item: the K and V rows are staged in the no-swizzle
 // K-major layout (norms accumulated on the way), the elected thread issues the rotation
@@ -26,7 +29,10 @@
 
 #include <cstdint>
 
+#include <cuda_fp16.h>
+
 #include "dev_common.cuh"
+#include "exact.cuh"
 #include "layout.cuh"
 #include "tq_internal.h"
 
@@ -42,10 +48,13 @@ constexpr int OFF_B = 0;                       // Pi_hi, Pi_lo, S'_hi, S'_lo: 4 
 constexpr int B_BYTES = 4 * 128 * 256;
 constexpr int OFF_K = OFF_B + B_BYTES;         // K rows (32 KB), later key-code staging unused
 constexpr int OFF_V = OFF_K + 128 * 256;       // V rows (32 KB), later value-code staging
-constexpr int OFF_NK = OFF_V + 128 * 256;      // [128] f32
-constexpr int OFF_NV = OFF_NK + 512;           // [128] f32
-constexpr int OFF_CB = OFF_NV + 512;           // ck[16] tk[16] cv[32] tv[32] f32
-constexpr int OFF_MBAR = OFF_CB + 96 * 4;      // blob, mma
+constexpr int OFF_NK = OFF_V + 128 * 256;      // [128] f32  ||k|| (stored)
+constexpr int OFF_NV = OFF_NK + 512;           // [128] f32  ||v|| (stored)
+constexpr int OFF_SK = OFF_NV + 512;           // [128] f32  256 ||2^s k||: yhat = Y / this
+constexpr int OFF_SV = OFF_SK + 512;           // [128] f32  256 ||2^s v||
+constexpr int OFF_EK = OFF_SV + 512;           // [128] i32  s of each key row
+constexpr int OFF_CB = OFF_EK + 512;           // ck[16] tk[16] cv[32] tv[32] nk[32] nv[64] f32
+constexpr int OFF_MBAR = OFF_CB + 192 * 4;     // blob, mma
 constexpr int OFF_MISC = OFF_MBAR + 16;        // tmem base, fail flag
 constexpr int SMEM = OFF_MISC + 16;
 // tensor memory columns
@@ -57,7 +66,8 @@ struct QArgs {
   int kv_heads, n_tokens, max_tokens, pages_per_seq, batch, items_per_seq;
   const int32_t* start_pos;
   uint8_t* cache;
-  const uint8_t* blob;   // bf16 operand blob, canonical layout
+  const uint8_t* blob;   // fp16 operand blob, canonical layout
+  const float* exact;    // exact-decision tables
   const float* ck;
   const float* tk;
   const float* cv;
@@ -65,12 +75,33 @@ struct QArgs {
   int* status;
 };
 
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+__device__ __forceinline__ float bf16_val(uint32_t bits) { return __uint_as_float(bits << 16); }
+// 2^e for e in [-126, 127]
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+// largest biased exponent among the 8 bf16 values of a 16-byte chunk
+__device__ __forceinline__ uint32_t max_exp8(uint4 w) {
+  const uint32_t a = max((w.x >> 7) & 0xFFu, (w.x >> 23) & 0xFFu), b = max((w.y >> 7) & 0xFFu, (w.y >> 23) & 0xFFu);
+  const uint32_t c = max((w.z >> 7) & 0xFFu, (w.z >> 23) & 0xFFu), d = max((w.w >> 7) & 0xFFu, (w.w >> 23) & 0xFFu);
+  return max(max(a, b), max(c, d));
 }
-__device__ __forceinline__ float bf16_val(uint32_t bits) {
-  return __bfloat162float(__ushort_as_bfloat16((unsigned short)bits));
+// 8 bf16 values times 2^s as fp16 (exact unless below fp16's normal range), and their sum of
+// squares added to acc
+__device__ __forceinline__ uint4 scale_to_f16(uint4 w, float f, float& acc) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float x0 = bf16_val(in[i] & 0xFFFFu) * f, x1 = bf16_val(in[i] >> 16) * f;
+    acc = fmaf(x0, x0, fmaf(x1, x1, acc));
+    out[i] = h2_bits(__floats2half2_rn(x0, x1));
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
 }
+// scaled residual of one key coordinate (kept as one expression for the fix-up path)
+__device__ __forceinline__ float key_resid(float yv, float nk, float c, float g) { return (yv - nk * c) * g; }
+// bit of coordinate j inside its key-code / sign word (page layout, head_dim 128)
+__device__ __forceinline__ int kbit(int j) { return 2 * (j >> 5) + ((j >> 4) & 1) + 8 * (j & 3); }
 
 template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
@@ -82,10 +113,16 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
   uint8_t* sV = smem + OFF_V;
   float* sNk = reinterpret_cast<float*>(smem + OFF_NK);
   float* sNv = reinterpret_cast<float*>(smem + OFF_NV);
+  float* sSk = reinterpret_cast<float*>(smem + OFF_SK);
+  float* sSv = reinterpret_cast<float*>(smem + OFF_SV);
+  int* sEk = reinterpret_cast<int*>(smem + OFF_EK);
   float* s_ck = reinterpret_cast<float*>(smem + OFF_CB);
   float* s_tk = s_ck + 16;
   float* s_cv = s_tk + 16;
   float* s_tv = s_cv + 32;
+  const float2* s_nk = reinterpret_cast<const float2*>(s_tv + 32);   // near tables, one float2 per cell
+  const float2* s_nv = s_nk + 16;
+  const exact::Tables T = exact::tables(a.exact, 128);
   uint64_t* bar_blob = reinterpret_cast<uint64_t*>(smem + OFF_MBAR);
   uint64_t* bar_mma = bar_blob + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
@@ -107,6 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
   for (int i = tid; i < LK - 1; i += kThreads) s_tk[i] = a.tk[i];
   for (int i = tid; i < LV; i += kThreads) s_cv[i] = a.cv[i];
   for (int i = tid; i < LV - 1; i += kThreads) s_tv[i] = a.tv[i];
+  for (int i = tid; i < 2 * LK; i += kThreads) s_tv[32 + i] = T.nkt[i];
+  for (int i = tid; i < 2 * LV; i += kThreads) s_tv[64 + i] = T.nvt[i];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -118,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
   }
   if (!mbar_wait(bar_blob, 0)) *s_fail = 1;
   uint32_t n_mma = 0;   // commits on bar_mma so far
-  constexpr uint32_t idesc = make_idesc(1, 1, 128, 128);   // bf16 x bf16 -> f32, M = N = 128
+  constexpr uint32_t idesc = make_idesc(0, 0, 128, 128);   // f16 x f16 -> f32, M = N = 128
   const uint32_t sB_addr = smem_u32(sB), sK_addr = smem_u32(sK), sV_addr = smem_u32(sV);
 
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -167,26 +206,31 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
         xk = __ldg(reinterpret_cast<const uint4*>(kseq + tok * D) + kc);
         xv = __ldg(reinterpret_cast<const uint4*>(vseq + tok * D) + kc);
       }
-      const uint32_t off = canon_off(slot, 16 * kc, 256);
-      *reinterpret_cast<uint4*>(sK + off) = xk;
-      *reinterpret_cast<uint4*>(sV + off) = xv;
-      float sk = 0.f, sv = 0.f;
-      const uint32_t wk[4] = {xk.x, xk.y, xk.z, xk.w}, wv[4] = {xv.x, xv.y, xv.z, xv.w};
+      // the row's scale 2^s: its largest magnitude into [2^14, 2^15) (the 16 chunks of a slot
+      // are 16 consecutive lanes)
+      uint32_t ek = max_exp8(xk), ev = max_exp8(xv);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float k0 = bf16_val(wk[i] & 0xFFFF), k1 = bf16_val(wk[i] >> 16);
-        const float v0 = bf16_val(wv[i] & 0xFFFF), v1 = bf16_val(wv[i] >> 16);
-        sk = fmaf(k0, k0, fmaf(k1, k1, sk));
-        sv = fmaf(v0, v0, fmaf(v1, v1, sv));
+      for (int o = 8; o > 0; o >>= 1) {
+        ek = max(ek, __shfl_xor_sync(0xffffffffu, ek, o));
+        ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, o));
       }
+      const int sk = min(141 - (int)ek, 126), sv = min(141 - (int)ev, 126);
+      float nk2 = 0.f, nv2 = 0.f;
+      const uint32_t off = canon_off(slot, 16 * kc, 256);
+      *reinterpret_cast<uint4*>(sK + off) = scale_to_f16(xk, exp2i(sk), nk2);
+      *reinterpret_cast<uint4*>(sV + off) = scale_to_f16(xv, exp2i(sv), nv2);
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {   // the 16 chunks of a slot are 16 consecutive lanes
-        sk += __shfl_xor_sync(0xffffffffu, sk, o);
-        sv += __shfl_xor_sync(0xffffffffu, sv, o);
+      for (int o = 8; o > 0; o >>= 1) {
+        nk2 += __shfl_xor_sync(0xffffffffu, nk2, o);
+        nv2 += __shfl_xor_sync(0xffffffffu, nv2, o);
       }
       if (kc == 0) {
-        sNk[slot] = sqrtf(sk);
-        sNv[slot] = sqrtf(sv);
+        const float rk = sqrtf(nk2), rv = sqrtf(nv2);
+        sNk[slot] = ldexpf(rk, -sk);
+        sNv[slot] = ldexpf(rv, -sv);
+        sSk[slot] = 256.f * rk;
+        sSv[slot] = 256.f * rv;
+        sEk[slot] = sk;
       }
     }
     fence_proxy_async();
@@ -214,15 +258,21 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
     uint32_t kwords[BK][4];   // key-code plane words of this slot
     float gamma2 = 0.f;
     if (warp < 4) {
-      // ---------- keys: codes, residual in the rotated frame, bf16 split into tensor memory ----------
+      // ---------- keys: codes, residual in the rotated frame, fp16 split into tensor memory ----------
 #pragma unroll
       for (int q = 0; q < BK; ++q)
 #pragma unroll
         for (int w = 0; w < 4; ++w) kwords[q][w] = 0u;
-      const float n = sNk[row];
-      const float inv = n > 0.f ? 1.f / n : 0.f;
-#pragma unroll
+      const float nk = sSk[row];   // Y / nk = yhat
+      const float inv = nk > 0.f ? 1.f / nk : 0.f;
+      // the residual's fp16 scale: |Y - nk c| <= 2 nk, brought below 2^15
+      const int en = (int)((__float_as_uint(nk) >> 23) & 0xFFu) - 127;
+      const float g = exp2i(max(-126, min(126, 13 - en)));
+      // chunks of 32 coordinates: coordinate c0 + i sits in word (i >> 2) & 3 at bit
+      // 2 (c0 >> 5) + ((i >> 4) & 1) + 8 (i & 3)
+#pragma unroll 1
       for (int c0 = 0; c0 < 128; c0 += 32) {
+        const int kb0 = 2 * (c0 >> 5);
         uint32_t y[32];
         {
           uint32_t t0[16], t1[16];
@@ -235,55 +285,119 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
             y[16 + i] = t1[i];
           }
         }
-        uint32_t rh[16], rl[16];
+        uint32_t rh[16], rl[16], near = 0u;
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           float r2[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int j = c0 + i + u;
             const float yv = __uint_as_float(y[i + u]);
             const float yh = yv * inv;
             int idx = 0;
 #pragma unroll
             for (int t = 0; t < LK - 1; ++t) idx += (yh >= s_tk[t]) ? 1 : 0;
-            // bit position of coordinate j inside its key-code word (layout of the page format)
-            const int w = (j >> 2) & 3, bit = 2 * (j >> 5) + ((j >> 4) & 1) + 8 * (j & 3);
+            const float2 cw = s_nk[idx];
+            near |= (fabsf(yh - cw.x) > cw.y ? 1u : 0u) << (i + u);
+            const int w = ((i + u) >> 2) & 3, bit = kb0 + (((i + u) >> 4) & 1) + 8 * ((i + u) & 3);
 #pragma unroll
             for (int q = 0; q < BK; ++q) kwords[q][w] |= (uint32_t)((idx >> q) & 1) << bit;
-            r2[u] = yv - n * s_ck[idx];
+            r2[u] = key_resid(yv, nk, s_ck[idx], g);
             gamma2 = fmaf(r2[u], r2[u], gamma2);
           }
-          const uint32_t h0 = bf16_bits(r2[0]), h1 = bf16_bits(r2[1]);
-          const uint32_t l0 = bf16_bits(r2[0] - bf16_val(h0)), l1 = bf16_bits(r2[1] - bf16_val(h1));
-          rh[i >> 1] = h0 | (h1 << 16);
-          rl[i >> 1] = l0 | (l1 << 16);
+          const __half2 h = __floats2half2_rn(r2[0], r2[1]);
+          rh[i >> 1] = h2_bits(h);
+          rl[i >> 1] = h2_bits(__floats2half2_rn(r2[0] - __low2float(h), r2[1] - __high2float(h)));
         }
         tmem_st16(tl + T_RHI + (c0 >> 1), rh);
         tmem_st16(tl + T_RLO + (c0 >> 1), rl);
+        if (!(nk > 0.f)) near = 0u;
+        uint32_t lanes = __ballot_sync(0xffffffffu, near != 0u);
+        if (lanes) {
+          // codes next to a boundary: exact decision, then the row's words, residual and gamma
+          tc_wait_st();
+          while (lanes) {
+            const int L = __ffs(lanes) - 1;
+            lanes &= lanes - 1;
+            uint32_t m = __shfl_sync(0xffffffffu, near, L);
+            float x[4];
+            exact::load_row<128>(kseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * D, lane, x);
+            const exact::F2 n = exact::norm<128>(x);
+            while (m) {
+              const int j = c0 + __ffs(m) - 1;
+              m &= m - 1;
+              const int idx2 = exact::code<128>(x, n, T.pih, T.pil, j, T.tkh, T.tkl, LK - 1, lane);
+              const uint32_t yj = tmem_ld1(tl + T_YK + j);
+              uint32_t hc = tmem_ld1(tl + T_RHI + (j >> 1)), lc = tmem_ld1(tl + T_RLO + (j >> 1));
+              tc_wait_ld();
+              if (lane == L) {
+                const float yv = __uint_as_float(yj), yh = yv * inv;
+                int idx = 0;
+#pragma unroll
+                for (int t = 0; t < LK - 1; ++t) idx += (yh >= s_tk[t]) ? 1 : 0;
+                if (idx != idx2) {
+                  const int w = (j >> 2) & 3, bit = kbit(j);
+#pragma unroll
+                  for (int q = 0; q < BK; ++q)
+#pragma unroll
+                    for (int ww = 0; ww < 4; ++ww)
+                      if (ww == w)
+                        kwords[q][ww] = (kwords[q][ww] & ~(1u << bit)) | ((uint32_t)((idx2 >> q) & 1) << bit);
+                  const float r0 = key_resid(yv, nk, s_ck[idx], g), r1 = key_resid(yv, nk, s_ck[idx2], g);
+                  gamma2 = fmaf(r1, r1, fmaf(-r0, r0, gamma2));
+                  const __half h = __float2half_rn(r1);
+                  const __half l = __float2half_rn(r1 - __half2float(h));
+                  const int sh = 16 * (j & 1);
+                  hc = (hc & ~(0xFFFFu << sh)) | ((uint32_t)__half_as_ushort(h) << sh);
+                  lc = (lc & ~(0xFFFFu << sh)) | ((uint32_t)__half_as_ushort(l) << sh);
+                }
+              }
+              tmem_st1(tl + T_RHI + (j >> 1), hc);
+              tmem_st1(tl + T_RLO + (j >> 1), lc);
+              tc_wait_st();
+            }
+          }
+        }
       }
       tc_wait_st();
     } else {
       // ---------- values: codes into the byte staging (slot-major rows, padded) ----------
-      const float n = sNv[row];
-      const float inv = n > 0.f ? 1.f / n : 0.f;
+      const float nv = sSv[row];
+      const float inv = nv > 0.f ? 1.f / nv : 0.f;
       uint8_t* dst = sV + row * kRowPad;   // sV's rows were consumed by the MMAs
 #pragma unroll 1
       for (int c0 = 0; c0 < 128; c0 += 16) {
         uint32_t y[16];
         tmem_ld16(tl + T_YV + c0, y);
         tc_wait_ld();
-        uint32_t packed[4] = {0u, 0u, 0u, 0u};
+        uint32_t packed[4] = {0u, 0u, 0u, 0u}, near = 0u;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float yh = __uint_as_float(y[i]) * inv;
           int idx = 0;
 #pragma unroll
           for (int t = 0; t < LV - 1; ++t) idx += (yh >= s_tv[t]) ? 1 : 0;
+          const float2 cw = s_nv[idx];
+          near |= (fabsf(yh - cw.x) > cw.y ? 1u : 0u) << i;
           packed[i >> 2] |= (uint32_t)idx << (8 * (i & 3));
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(dst + c0 + 4 * i) = packed[i];
+        if (!(nv > 0.f)) near = 0u;
+        uint32_t lanes = __ballot_sync(0xffffffffu, near != 0u);
+        while (lanes) {   // codes next to a boundary: exact decision
+          const int L = __ffs(lanes) - 1;
+          lanes &= lanes - 1;
+          uint32_t m = __shfl_sync(0xffffffffu, near, L);
+          float x[4];
+          exact::load_row<128>(vseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * D, lane, x);
+          const exact::F2 n = exact::norm<128>(x);
+          while (m) {
+            const int j = c0 + __ffs(m) - 1;
+            m &= m - 1;
+            const int idx2 = exact::code<128>(x, n, T.pih, T.pil, j, T.tvh, T.tvl, LV - 1, lane);
+            if (lane == L) dst[j] = (uint8_t)idx2;
+          }
+        }
       }
     }
     tc_fence_before();
@@ -306,16 +420,50 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
       if (!mbar_wait(bar_mma, (n_mma - 1) & 1)) *s_fail = 1;
       tc_fence_after();
       uint32_t swords[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
+      // z = 256 sum_j (g 2^s r_j) S'[i][j]: near zero when within kDeltaSign ||r|| in those units
+      const float zthr = exact::kDeltaSign * 256.f * sqrtf(gamma2);
+#pragma unroll 1
       for (int c0 = 0; c0 < 128; c0 += 16) {
         uint32_t z[16];
         tmem_ld16(tl + T_Z + c0, z);
         tc_wait_ld();
+        uint32_t near = 0u;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = c0 + i;
-          const int w = (j >> 2) & 3, bit = 2 * (j >> 5) + ((j >> 4) & 1) + 8 * (j & 3);
-          swords[w] |= (__uint_as_float(z[i]) >= 0.f ? 1u : 0u) << bit;
+        for (int i = 0; i < 16; ++i) {   // c0 % 16 == 0: word (i >> 2) & 3
+          const float zv = __uint_as_float(z[i]);
+          swords[(i >> 2) & 3] |= (zv >= 0.f ? 1u : 0u) << (2 * (c0 >> 5) + ((c0 >> 4) & 1) + 8 * (i & 3));
+          near |= (fabsf(zv) < zthr ? 1u : 0u) << i;
+        }
+        uint32_t lanes = __ballot_sync(0xffffffffu, near != 0u);
+        while (lanes) {   // projections next to zero: exact sign
+          const int L = __ffs(lanes) - 1;
+          lanes &= lanes - 1;
+          uint32_t m = __shfl_sync(0xffffffffu, near, L);
+          // this lane's 4 codes (coordinates 4 lane + e) of row L: word lane & 3 of each plane
+          int codes[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int q = 0; q < BK; ++q) {
+            const uint32_t w0 = __shfl_sync(0xffffffffu, kwords[q][0], L), w1 = __shfl_sync(0xffffffffu, kwords[q][1], L);
+            const uint32_t w2 = __shfl_sync(0xffffffffu, kwords[q][2], L), w3 = __shfl_sync(0xffffffffu, kwords[q][3], L);
+            const int w = lane & 3;
+            const uint32_t kw = w == 0 ? w0 : w == 1 ? w1 : w == 2 ? w2 : w3;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) codes[e] |= (int)((kw >> kbit(4 * lane + e)) & 1u) << q;
+          }
+          float x[4];
+          exact::load_row<128>(kseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * D, lane, x);
+          const exact::F2 n = exact::norm<128>(x);
+          while (m) {
+            const int i = c0 + __ffs(m) - 1;
+            m &= m - 1;
+            const bool sg = exact::sign<128>(x, n, codes, T.sh, T.sl, T.qh, T.ql, T.ckh, T.ckl, i, lane);
+            if (lane == L) {
+              const int w = (i >> 2) & 3, bit = kbit(i);
+#pragma unroll
+              for (int ww = 0; ww < 4; ++ww)
+                if (ww == w) swords[ww] = (swords[ww] & ~(1u << bit)) | ((sg ? 1u : 0u) << bit);
+            }
+          }
         }
       }
       if (valid) {
@@ -327,7 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
         *reinterpret_cast<uint4*>(pg + PL::off_signs + (size_t)row * 16) =
             make_uint4(swords[0], swords[1], swords[2], swords[3]);
         reinterpret_cast<float*>(pg + PL::off_nk)[row] = sNk[row];
-        reinterpret_cast<float*>(pg + PL::off_gamma)[row] = sqrtf(gamma2);
+        // gamma = ||g 2^(s+8) r|| / (g 2^(s+8)), g = 2^(13 - exponent of nk)
+        const int en = (int)((__float_as_uint(sSk[row]) >> 23) & 0xFFu) - 127;
+        reinterpret_cast<float*>(pg + PL::off_gamma)[row] =
+            ldexpf(sqrtf(gamma2), -(sEk[row] + 8) - max(-126, min(126, 13 - en)));
         reinterpret_cast<float*>(pg + PL::off_nv)[row] = sNv[row];
       }
     } else {
@@ -386,6 +537,7 @@ int launch(const tq_ctx* c, const void* k, const void* v, int batch, int kv_head
   a.start_pos = start_pos;
   a.cache = static_cast<uint8_t*>(cache);
   a.blob = c->d_qblob;
+  a.exact = c->d_exact;
   a.ck = c->d_ck;
   a.tk = c->d_tk;
   a.cv = c->d_cv;

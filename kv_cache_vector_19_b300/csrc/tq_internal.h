@@ -56,14 +56,17 @@ struct tq_ctx {
   float* d_cv = nullptr;    // [lv]
   float* d_tv = nullptr;    // [lv-1]
   int* d_status = nullptr;  // sticky flags
+  // double-float tables of the exact boundary decisions (exact.cuh: Pi, S, S' as hi + lo,
+  // boundaries and key centroids as hi + lo, near tables)
+  float* d_exact = nullptr;
   // bit-plane expansion of the books: c[idx] = 2 sum_M alpha_M x_M(idx) - sum_M alpha_M
   float* d_alpha_k = nullptr;   // [2^(bits-2)]
   float* d_alpha_v = nullptr;   // [2^(bits-1)]
   float asum_k = 0.f, asum_v = 0.f;
   int num_sms = 148;
   int decode_path = 0;   // TQ_DECODE_*
-  // head_dim 128: bf16 B operands of the tensor-core quantizer, no-swizzle K-major layout:
-  // Pi hi, Pi lo, S' hi, S' lo (each 128 x 128, 32 KB)
+  // head_dim 128: fp16 B operands of the tensor-core quantizer, no-swizzle K-major layout:
+  // 256 Pi as hi, lo and 256 S' as hi, lo (each 128 x 128, 32 KB)
   uint8_t* d_qblob = nullptr;
 };
 

@@ -1,11 +1,14 @@
 """Shared helpers of the GPU parity tests: run the library through its C ABI, run the
 oracle on the same seeded inputs, and compare them under the acceptance bars.
 
-Bars (from the method's acceptance statement):
+Bars (from the method's acceptance statement, the first two made stricter):
   * packing and indexing bit-exact (the oracle's own packer re-packs the GPU's codes into
     identical page bytes);
-  * code + sign mismatch rate <= 1e-4, and every mismatch within a hair of a quantizer
-    boundary (|yhat - t_k| < 1e-3/sqrt(d), or |(S r)_i| < 1e-3 * gamma);
+  * codes and signs identical to the oracle's.  The statement allows a mismatch rate of
+    1e-4 with every flip at a quantizer boundary; the library takes every decision that its
+    fast arithmetic puts near a boundary again in double-float arithmetic, so its codes are
+    those of exact arithmetic and no flip is expected.  The near-boundary rule stays checked
+    (|yhat - t_k| < 1e-3/sqrt(d), or |(S r)_i| < 1e-3 * gamma) for any rate passed in;
   * logits within 2e-3 absolute of the oracle's logits on the GPU's own pages;
   * decode outputs within 1e-2 relative L2 of the oracle's quantize + decode.
 """
@@ -16,7 +19,7 @@ import kv_cache_vector_19_b300 as tq
 from oracle import decode as odec
 from oracle import pagefmt, params, quant
 
-MISMATCH_RATE = 1e-4
+MISMATCH_RATE = 0.0
 LOGIT_ATOL = 2e-3
 OUT_REL_L2 = 1e-2
 # Decode against the oracle on the GPU's own pages (no quantizer flips): only the decode

@@ -162,7 +162,9 @@ def test_append_one_token_at_a_time_matches_bulk():
             sl = slice(250, 260)
             got = {key: val[sl] for key, val in tc.items()}
             res = P.compare_sequence(step, P.to64(k[bb, h, sl]), P.to64(v[bb, h, sl]), got)
-            P.assert_quantize_ok(res, rate=1e-3)
+            P.assert_quantize_ok(res)
+            for key in ("kidx", "vidx", "sigma"):   # exact decisions on both paths
+                assert np.array_equal(tc[key][sl], ta[key][sl]), key
             for key in ("nk", "nv", "gamma"):
                 assert np.allclose(tc[key][sl], ta[key][sl], rtol=1e-5, atol=1e-30), key
 
