@@ -501,6 +501,43 @@ def run_sweep(args):
     return 0
 
 
+def run_case(args, w):
+    """One kernel of the workload, alone, at a reduced prefill length: the cases the ncu
+    summaries under profiles/ are taken on.  --kernel-case quantize runs tq_quantize_kv of the
+    prefill; decode runs tq_attn_decode over it.  warmup + steps calls, no JSON line."""
+    import torch
+
+    import kv_cache_vector_19_b300 as tq
+    from kv_cache_vector_19_b300 import workloads
+
+    wl = workloads.preset(w.name, tokens=args.tokens or w.tokens, decode_steps=1)
+    data = workloads.generate(wl)
+    B, H, Hq, T, d = wl.batch, wl.kv_heads, wl.q_heads, wl.tokens, wl.d
+    ctx = tq.Context(d, wl.b, seed=wl.seed)
+    cache = ctx.alloc_cache(B, H, T)
+    k, v = data["k"].cuda(), data["v"].cuda()
+    zero = torch.zeros(B, dtype=torch.int32, device="cuda")
+    calls = args.warmup + args.steps
+    if args.kernel_case == "quantize":
+        for _ in range(calls):
+            ctx.quantize_kv(k, v, zero, cache, T)
+    else:
+        ctx.quantize_kv(k, v, zero, cache, T)
+        ws = ctx.alloc_workspace(B, Hq, H, T)
+        q = data["q"][0].cuda().contiguous()
+        out = torch.empty_like(q)
+        lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        for _ in range(calls):
+            ctx.attn_decode(q, cache, lens, H, T, out, ws)
+    torch.cuda.synchronize()
+    st = ctx.device_status()
+    ctx.close()
+    if st != tq.TQ_OK:
+        raise SystemExit(f"device status: {tq.tq_status_string(st)}")
+    print(f"{args.kernel_case} case: {w.name}, {T} tokens, {calls} calls, status ok", flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -510,6 +547,9 @@ def main():
     ap.add_argument("--workload", default="longctx", choices=["longctx", "llama8b", "llama70b", "tiny"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-case", choices=["quantize", "decode"], default=None,
+                    help="run one kernel of the workload alone (profiling case), no JSON line")
+    ap.add_argument("--tokens", type=int, default=0, help="prefill length of --kernel-case (default: workload's)")
     args = ap.parse_args()
     if args.warmup < 3 and not args.sweep:
         args.warmup = 3
@@ -519,6 +559,8 @@ def main():
         return run_reference(args, w)
     if args.sweep:
         return run_sweep(args)
+    if args.kernel_case:
+        return run_case(args, w)
     return run_ours(args, w)
 
 

@@ -135,6 +135,144 @@ __device__ __forceinline__ int code(const float* x, F2 n, const float* __restric
   return __popc(__ballot_sync(0xffffffffu, ge));
 }
 
+// E consecutive fp32 values at p (E = 2, 4 or 8), 8-byte aligned.
+template <int E>
+__device__ __forceinline__ void load_f(const float* __restrict__ p, float* v) {
+  if constexpr (E == 2) {
+    const float2 a = *reinterpret_cast<const float2*>(p);
+    v[0] = a.x;
+    v[1] = a.y;
+  } else {
+#pragma unroll
+    for (int g = 0; g < E / 2; ++g) {
+      const float2 a = *reinterpret_cast<const float2*>(p + 2 * g);
+      v[2 * g] = a.x;
+      v[2 * g + 1] = a.y;
+    }
+  }
+}
+
+// code() for the vector at `row` (global bf16), every load issued before the arithmetic so
+// that one memory round trip serves the whole decision; ||x|| = 0 gives the middle code.
+template <int D>
+__device__ __forceinline__ int code_of_row(const __nv_bfloat16* row, const float* __restrict__ pih,
+                                           const float* __restrict__ pil, int j, const float* __restrict__ th,
+                                           const float* __restrict__ tl, int nb, int lane) {
+  constexpr int E = D / 32;
+  float x[E], ph[E], pl[E];
+  load_row<D>(row, lane, x);
+  load_f<E>(pih + (size_t)j * D + lane * E, ph);
+  load_f<E>(pil + (size_t)j * D + lane * E, pl);
+  const float bh = lane < nb ? th[lane] : 0.f, bl = lane < nb ? tl[lane] : 0.f;
+  const F2 n = norm<D>(x);
+  if (!(n.hi > 0.f)) return (nb + 1) / 2;
+  F2 y{0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < E; ++e) y = add(y, mul_f(F2{ph[e], pl[e]}, x[e]));
+  y = warp_sum(y);
+  const bool ge = lane < nb && nonneg(add(y, neg(mul(F2{bh, bl}, n))));
+  return __popc(__ballot_sync(0xffffffffu, ge));
+}
+
+// sign() for the vector at `row` with the lane's E codes, loads first as in code_of_row.
+template <int D>
+__device__ __forceinline__ bool sign_of_row(const __nv_bfloat16* row, const int* codes,
+                                            const float* __restrict__ sh, const float* __restrict__ sl,
+                                            const float* __restrict__ qh, const float* __restrict__ ql,
+                                            const float* __restrict__ ch, const float* __restrict__ cl, int i,
+                                            int lane) {
+  constexpr int E = D / 32;
+  float x[E], s_h[E], s_l[E], q_h[E], q_l[E], c_h[E], c_l[E];
+  load_row<D>(row, lane, x);
+  const size_t o = (size_t)i * D + lane * E;
+  load_f<E>(sh + o, s_h);
+  load_f<E>(sl + o, s_l);
+  load_f<E>(qh + o, q_h);
+  load_f<E>(ql + o, q_l);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    c_h[e] = ch[codes[e]];
+    c_l[e] = cl[codes[e]];
+  }
+  const F2 n = norm<D>(x);
+  F2 a{0.f, 0.f}, b{0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    a = add(a, mul_f(F2{s_h[e], s_l[e]}, x[e]));
+    b = add(b, mul(F2{q_h[e], q_l[e]}, F2{c_h[e], c_l[e]}));
+  }
+  a = warp_sum(a);
+  b = warp_sum(b);
+  return nonneg(add(a, neg(mul(n, b))));
+}
+
+// Two-step forms for callers that hide the memory round trip: pre_*() issues every load of
+// one decision into registers (warp-collective, no arithmetic), fin_*() takes it later.
+// head_dim 128 (4 coordinates per lane); the bf16 values stay packed until they are used.
+struct CodePre {
+  uint2 xb;
+  float ph[4], pl[4], bh, bl;
+};
+__device__ __forceinline__ void unpack4(uint2 w, float* x) {
+  x[0] = __uint_as_float(w.x << 16);
+  x[1] = __uint_as_float(w.x & 0xFFFF0000u);
+  x[2] = __uint_as_float(w.y << 16);
+  x[3] = __uint_as_float(w.y & 0xFFFF0000u);
+}
+__device__ __forceinline__ void pre_code(CodePre& p, const __nv_bfloat16* row, const float* __restrict__ pih,
+                                         const float* __restrict__ pil, int j, const float* __restrict__ th,
+                                         const float* __restrict__ tl, int nb, int lane) {
+  p.xb = *reinterpret_cast<const uint2*>(row + lane * 4);
+  load_f<4>(pih + (size_t)j * 128 + lane * 4, p.ph);
+  load_f<4>(pil + (size_t)j * 128 + lane * 4, p.pl);
+  p.bh = lane < nb ? th[lane] : 0.f;
+  p.bl = lane < nb ? tl[lane] : 0.f;
+}
+__device__ __forceinline__ int fin_code(const CodePre& p, int nb, int lane) {
+  float x[4];
+  unpack4(p.xb, x);
+  const F2 n = norm<128>(x);
+  if (!(n.hi > 0.f)) return (nb + 1) / 2;
+  F2 y{0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) y = add(y, mul_f(F2{p.ph[e], p.pl[e]}, x[e]));
+  y = warp_sum(y);
+  const bool ge = lane < nb && nonneg(add(y, neg(mul(F2{p.bh, p.bl}, n))));
+  return __popc(__ballot_sync(0xffffffffu, ge));
+}
+struct SignPre {
+  uint2 xb;
+  float sh[4], sl[4], qh[4], ql[4];
+  uint32_t codes;   // the lane's 4 codes, 8 bits each
+};
+__device__ __forceinline__ void pre_sign(SignPre& p, const __nv_bfloat16* row, uint32_t codes,
+                                         const float* __restrict__ sh, const float* __restrict__ sl,
+                                         const float* __restrict__ qh, const float* __restrict__ ql, int i, int lane) {
+  p.xb = *reinterpret_cast<const uint2*>(row + lane * 4);
+  const size_t o = (size_t)i * 128 + lane * 4;
+  load_f<4>(sh + o, p.sh);
+  load_f<4>(sl + o, p.sl);
+  load_f<4>(qh + o, p.qh);
+  load_f<4>(ql + o, p.ql);
+  p.codes = codes;
+}
+// ch / cl: the centroids as hi + lo (shared memory)
+__device__ __forceinline__ bool fin_sign(const SignPre& p, const float* ch, const float* cl) {
+  float x[4];
+  unpack4(p.xb, x);
+  const F2 n = norm<128>(x);
+  F2 a{0.f, 0.f}, b{0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int c = (int)((p.codes >> (8 * e)) & 0xFFu);
+    a = add(a, mul_f(F2{p.sh[e], p.sl[e]}, x[e]));
+    b = add(b, mul(F2{p.qh[e], p.ql[e]}, F2{ch[c], cl[c]}));
+  }
+  a = warp_sum(a);
+  b = warp_sum(b);
+  return nonneg(add(a, neg(mul(n, b))));
+}
+
 // QJL bit of projection row i: (S r)_i >= 0 with r = x - ||x|| Pi^T c[idx], taken as
 // (S x)_i - ||x|| (S' c[idx])_i, S' = S Pi^T (equal in exact arithmetic).  codes: the lane's
 // E codes of the vector; sh / sl: S row-major, qh / ql: S' row-major; ch / cl: centroids.

@@ -42,7 +42,6 @@ namespace qtc {
 using namespace dev;
 
 constexpr int kThreads = 256;
-constexpr int kRowPad = 132;   // bytes per slot row of the value-code staging (bank-conflict free)
 // shared memory
 constexpr int OFF_B = 0;                       // Pi_hi, Pi_lo, S'_hi, S'_lo: 4 x 32 KB, canonical
 constexpr int B_BYTES = 4 * 128 * 256;
@@ -196,41 +195,54 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
         }
       }
     }
-#pragma unroll 4
-    for (int it = 0; it < 8; ++it) {
-      const int c = tid + kThreads * it;   // 16-byte chunk: slot c / 16, chunk c % 16
-      const int slot = c >> 4, kc = c & 15;
-      uint4 xk = make_uint4(0u, 0u, 0u, 0u), xv = make_uint4(0u, 0u, 0u, 0u);
-      if (slot >= lo && slot < hi) {
-        const long tok = (long)page * 128 + slot - start;
-        xk = __ldg(reinterpret_cast<const uint4*>(kseq + tok * D) + kc);
-        xv = __ldg(reinterpret_cast<const uint4*>(vseq + tok * D) + kc);
-      }
-      // the row's scale 2^s: its largest magnitude into [2^14, 2^15) (the 16 chunks of a slot
-      // are 16 consecutive lanes)
-      uint32_t ek = max_exp8(xk), ev = max_exp8(xv);
+    // 8 operand rows per warp and group; lane (s8, k4) takes 16-byte chunks k4, k4 + 4, ...
+    // (a store of the warp covers 8 rows x 64 bytes: conflict free).  K rows are in slot order;
+    // V row r holds slot slot_of(r >> 5, r & 31), so that the value coders' ballots are words.
+    {
+      const int s8 = lane & 7, k4 = lane >> 3;
+#pragma unroll 1
+      for (int grp = warp; grp < 16; grp += 8) {
+        const int r = 8 * grp + s8, vs = slot_of(r >> 5, r & 31);
+        const bool kval = r >= lo && r < hi, vval = vs >= lo && vs < hi;
+        const uint4* kp = reinterpret_cast<const uint4*>(kseq + ((long)page * 128 + r - start) * D);
+        const uint4* vp = reinterpret_cast<const uint4*>(vseq + ((long)page * 128 + vs - start) * D);
+        uint4 xk[4], xv[4];
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
-        ek = max(ek, __shfl_xor_sync(0xffffffffu, ek, o));
-        ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, o));
-      }
-      const int sk = min(141 - (int)ek, 126), sv = min(141 - (int)ev, 126);
-      float nk2 = 0.f, nv2 = 0.f;
-      const uint32_t off = canon_off(slot, 16 * kc, 256);
-      *reinterpret_cast<uint4*>(sK + off) = scale_to_f16(xk, exp2i(sk), nk2);
-      *reinterpret_cast<uint4*>(sV + off) = scale_to_f16(xv, exp2i(sv), nv2);
+        for (int q = 0; q < 4; ++q) {
+          xk[q] = kval ? __ldg(kp + k4 + 4 * q) : make_uint4(0u, 0u, 0u, 0u);
+          xv[q] = vval ? __ldg(vp + k4 + 4 * q) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        // the row's scale 2^s: its largest magnitude into [2^14, 2^15)
+        uint32_t ek = 0u, ev = 0u;
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
-        nk2 += __shfl_xor_sync(0xffffffffu, nk2, o);
-        nv2 += __shfl_xor_sync(0xffffffffu, nv2, o);
-      }
-      if (kc == 0) {
-        const float rk = sqrtf(nk2), rv = sqrtf(nv2);
-        sNk[slot] = ldexpf(rk, -sk);
-        sNv[slot] = ldexpf(rv, -sv);
-        sSk[slot] = 256.f * rk;
-        sSv[slot] = 256.f * rv;
-        sEk[slot] = sk;
+        for (int q = 0; q < 4; ++q) {
+          ek = max(ek, max_exp8(xk[q]));
+          ev = max(ev, max_exp8(xv[q]));
+        }
+        ek = max(ek, __shfl_xor_sync(0xffffffffu, ek, 8));
+        ek = max(ek, __shfl_xor_sync(0xffffffffu, ek, 16));
+        ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 8));
+        ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 16));
+        const int sk = min(141 - (int)ek, 126), sv = min(141 - (int)ev, 126);
+        float nk2 = 0.f, nv2 = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t off = canon_off(r, 16 * (k4 + 4 * q), 256);
+          *reinterpret_cast<uint4*>(sK + off) = scale_to_f16(xk[q], exp2i(sk), nk2);
+          *reinterpret_cast<uint4*>(sV + off) = scale_to_f16(xv[q], exp2i(sv), nv2);
+        }
+        nk2 += __shfl_xor_sync(0xffffffffu, nk2, 8);
+        nk2 += __shfl_xor_sync(0xffffffffu, nk2, 16);
+        nv2 += __shfl_xor_sync(0xffffffffu, nv2, 8);
+        nv2 += __shfl_xor_sync(0xffffffffu, nv2, 16);
+        if (k4 == 0) {
+          const float rk = sqrtf(nk2), rv = sqrtf(nv2);
+          sNk[r] = ldexpf(rk, -sk);   // by slot
+          sNv[r] = ldexpf(rv, -sv);   // by V row
+          sSk[r] = 256.f * rk;
+          sSv[r] = 256.f * rv;
+          sEk[r] = sk;
+        }
       }
     }
     fence_proxy_async();
@@ -319,13 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
             const int L = __ffs(lanes) - 1;
             lanes &= lanes - 1;
             uint32_t m = __shfl_sync(0xffffffffu, near, L);
-            float x[4];
-            exact::load_row<128>(kseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * D, lane, x);
-            const exact::F2 n = exact::norm<128>(x);
+            const __nv_bfloat16* xr = kseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * D;
             while (m) {
               const int j = c0 + __ffs(m) - 1;
               m &= m - 1;
-              const int idx2 = exact::code<128>(x, n, T.pih, T.pil, j, T.tkh, T.tkl, LK - 1, lane);
+              const int idx2 = exact::code_of_row<128>(xr, T.pih, T.pil, j, T.tkh, T.tkl, LK - 1, lane);
               const uint32_t yj = tmem_ld1(tl + T_YK + j);
               uint32_t hc = tmem_ld1(tl + T_RHI + (j >> 1)), lc = tmem_ld1(tl + T_RLO + (j >> 1));
               tc_wait_ld();
@@ -360,16 +370,20 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
       }
       tc_wait_st();
     } else {
-      // ---------- values: codes into the byte staging (slot-major rows, padded) ----------
-      const float nv = sSv[row];
+      // ---------- values: V row 32 c + lane holds slot slot_of(c, lane), so one ballot per
+      // (coordinate, plane) is the page word (plane, coordinate, c); lane i keeps coordinate c0 + i's ----------
+      const int c = warp & 3, vrow = 32 * c + lane, slot = slot_of(c, lane);
+      const float nv = sSv[vrow];
       const float inv = nv > 0.f ? 1.f / nv : 0.f;
-      uint8_t* dst = sV + row * kRowPad;   // sV's rows were consumed by the MMAs
+      const bool vvalid = slot >= lo && slot < hi;
+      const uint32_t vmask = __ballot_sync(0xffffffffu, vvalid);
+      uint32_t* g_vc = reinterpret_cast<uint32_t*>(pg + PL::off_vcodes);
 #pragma unroll 1
       for (int c0 = 0; c0 < 128; c0 += 16) {
         uint32_t y[16];
         tmem_ld16(tl + T_YV + c0, y);
         tc_wait_ld();
-        uint32_t packed[4] = {0u, 0u, 0u, 0u}, near = 0u;
+        uint32_t ib[4] = {0u, 0u, 0u, 0u}, near = 0u;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float yh = __uint_as_float(y[i]) * inv;
@@ -378,27 +392,51 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
           for (int t = 0; t < LV - 1; ++t) idx += (yh >= s_tv[t]) ? 1 : 0;
           const float2 cw = s_nv[idx];
           near |= (fabsf(yh - cw.x) > cw.y ? 1u : 0u) << i;
-          packed[i >> 2] |= (uint32_t)idx << (8 * (i & 3));
+          ib[i >> 2] |= (uint32_t)idx << (8 * (i & 3));
         }
+        uint32_t wv[BV];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(dst + c0 + 4 * i) = packed[i];
+        for (int p = 0; p < BV; ++p) wv[p] = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t idx = (ib[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+#pragma unroll
+          for (int p = 0; p < BV; ++p) {
+            const uint32_t bal = __ballot_sync(0xffffffffu, (idx >> p) & 1u);
+            if (lane == i) wv[p] = bal;
+          }
+        }
         if (!(nv > 0.f)) near = 0u;
         uint32_t lanes = __ballot_sync(0xffffffffu, near != 0u);
-        while (lanes) {   // codes next to a boundary: exact decision
+        while (lanes) {   // codes next to a boundary: exact decision, into the keeper lane's words
           const int L = __ffs(lanes) - 1;
           lanes &= lanes - 1;
           uint32_t m = __shfl_sync(0xffffffffu, near, L);
-          float x[4];
-          exact::load_row<128>(vseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * D, lane, x);
-          const exact::F2 n = exact::norm<128>(x);
+          const __nv_bfloat16* xr = vseq + ((long)page * 128 + __shfl_sync(0xffffffffu, slot, L) - start) * D;
           while (m) {
-            const int j = c0 + __ffs(m) - 1;
+            const int cc = __ffs(m) - 1;
             m &= m - 1;
-            const int idx2 = exact::code<128>(x, n, T.pih, T.pil, j, T.tvh, T.tvl, LV - 1, lane);
-            if (lane == L) dst[j] = (uint8_t)idx2;
+            const int idx2 = exact::code_of_row<128>(xr, T.pih, T.pil, c0 + cc, T.tvh, T.tvl, LV - 1, lane);
+            if (lane == cc) {
+#pragma unroll
+              for (int p = 0; p < BV; ++p) wv[p] = (wv[p] & ~(1u << L)) | ((uint32_t)((idx2 >> p) & 1) << L);
+            }
+          }
+        }
+        if (vmask && lane < 16) {
+#pragma unroll
+          for (int p = 0; p < BV; ++p) {
+            uint32_t* dst = g_vc + ((size_t)p * D + c0 + lane) * 4 + c;
+            if (vmask == 0xffffffffu) {
+              *dst = wv[p];
+            } else {
+              atomicAnd(dst, ~vmask);
+              atomicOr(dst, wv[p] & vmask);
+            }
           }
         }
       }
+      if (vvalid) reinterpret_cast<float*>(pg + PL::off_nv)[slot] = sNv[vrow];
     }
     tc_fence_before();
     __syncthreads();
@@ -450,13 +488,11 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) codes[e] |= (int)((kw >> kbit(4 * lane + e)) & 1u) << q;
           }
-          float x[4];
-          exact::load_row<128>(kseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * D, lane, x);
-          const exact::F2 n = exact::norm<128>(x);
+          const __nv_bfloat16* xr = kseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * D;
           while (m) {
             const int i = c0 + __ffs(m) - 1;
             m &= m - 1;
-            const bool sg = exact::sign<128>(x, n, codes, T.sh, T.sl, T.qh, T.ql, T.ckh, T.ckl, i, lane);
+            const bool sg = exact::sign_of_row<128>(xr, codes, T.sh, T.sl, T.qh, T.ql, T.ckh, T.ckl, i, lane);
             if (lane == L) {
               const int w = (i >> 2) & 3, bit = kbit(i);
 #pragma unroll
@@ -479,33 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
         const int en = (int)((__float_as_uint(sSk[row]) >> 23) & 0xFFu) - 127;
         reinterpret_cast<float*>(pg + PL::off_gamma)[row] =
             ldexpf(sqrtf(gamma2), -(sEk[row] + 8) - max(-126, min(126, 13 - en)));
-        reinterpret_cast<float*>(pg + PL::off_nv)[row] = sNv[row];
-      }
-    } else {
-      // value-code words [plane][coordinate][4], each over 32 slots of the page; the page
-      // layout puts slot tau = 32 kb + 16 h + 4 c + e at word c, bit 2 kb + h + 8 e
-      uint32_t* g_vc = reinterpret_cast<uint32_t*>(pg + PL::off_vcodes);
-      const int t4 = tid - 128;
-#pragma unroll 1
-      for (int e = t4; e < BV * D * 4; e += 128) {
-        const int plane = e / (D * 4), rem = e % (D * 4), j = rem >> 2, c = rem & 3;
-        uint32_t word = 0u, mask = 0u;
-#pragma unroll
-        for (int bit = 0; bit < 32; ++bit) {
-          const int kb = (bit & 7) >> 1, h = bit & 1, el = bit >> 3;
-          const int slot = 32 * kb + 16 * h + 4 * c + el;
-          if (slot >= lo && slot < hi) {
-            mask |= 1u << bit;
-            word |= (uint32_t)((sV[slot * kRowPad + j] >> plane) & 1) << bit;
-          }
-        }
-        uint32_t* dst = g_vc + ((size_t)plane * D + j) * 4 + c;
-        if (mask == 0xffffffffu) {
-          *dst = word;
-        } else if (mask != 0u) {
-          atomicAnd(dst, ~mask);
-          atomicOr(dst, word);
-        }
       }
     }
   }
