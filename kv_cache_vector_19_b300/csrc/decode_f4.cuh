@@ -44,14 +44,15 @@
 // MMAs.  Issuers never touch shared memory: a waiter warp polls the mbarriers (bounded
 // waits) and releases its issuers through a named barrier.
 //
-// Warp roles (21 warps):
-//   0-3, 16-19  token warps (two independent sets, each half of the query heads): D_s ->
+// Warp roles (21 warps with two token-warp sets, 29 with four):
+//   0-3, 16-19  token warps (independent sets, each a share of the query heads; further sets
+//               at 20-23, 24-27): D_s ->
 //               logits, lazy online softmax, D_v rescale when the running maximum moves,
 //               weights -> fixed-point pieces -> 8 x 8 nibble transposes -> B_v
 //   4-7         key-plane warps: key planes and sign plane -> A_s, token norms -> TMEM
 //   8-11        value-plane warps: value planes -> A_v; epilogue
 //   12          score-MMA issuer; 13, 14 value-MMA issuers
-//   15          score waiter; 20 value waiter and page ring (cp.async.bulk, L2 prefetch)
+//   15          score waiter; the last warp value waiter and page ring (cp.async.bulk, L2 prefetch)
 #pragma once
 
 #include <cuda_runtime.h>
@@ -79,7 +80,10 @@ constexpr int kWarpIV0 = 13;  // value-MMA issuer, first half of the planes
 constexpr int kWarpIV1 = 14;  // value-MMA issuer, second half
 constexpr int kWarpWS = 15;   // score waiter
 constexpr int kWarpT2 = 16;   // token warps, further sets (16-19, 20-23, ...), then the value waiter
-constexpr int kTokenSets = 2; // token-warp sets (each a warp per TMEM lane quarter); at most GP
+// Token-warp sets (each a warp per TMEM lane quarter, each owning GP / sets query heads): two
+// for up to 4 query heads per KV head, four from 8 on (measured on the long-context shapes:
+// G = 4 two sets 248 us, four 254 us; G = 8 two sets 446 us, four 340 us per call).
+__host__ __device__ constexpr int token_sets(int gp) { return gp >= 8 ? 4 : (gp < 2 ? gp : 2); }
 constexpr int kL2Ahead = 12;  // pages prefetched into L2 beyond the shared-memory ring
 constexpr int kRingMax = 8;   // ring slots (as many as fit, at most this; a streaming probe
                               // of this grid runs the whole cache through 4-8 slots at ~5 TB/s)
@@ -103,7 +107,7 @@ struct Cfg {
   using PL = PageLayout<128, BITS>;
   static constexpr int BK = BITS - 1, BV = BITS;
   static constexpr int PK = 1 << (BK - 1), PV = 1 << (BV - 1), NS = PK + 1;
-  static constexpr int TS = kTokenSets < GP ? kTokenSets : GP;   // token-warp sets
+  static constexpr int TS = token_sets(GP);          // token-warp sets
   static constexpr int HPT = GP / TS;                  // query heads per token-warp set
   static constexpr int WV = kWarpT2 + 4 * (TS - 1);    // value waiter; page ring
   static constexpr int WARPS = WV + 1;
