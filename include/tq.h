@@ -123,6 +123,21 @@ int tq_make_projection(int m, int d, uint64_t seed, double* s_out);
  * them to `device`.  Returns TQ_EUNSUPPORTED unless d in {64,128,256}, bits in 2..5 and
  * m == d.  The context is immutable afterwards and may be shared by concurrent calls. */
 int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, tq_ctx** out);
+
+/* Format version 2: separate key and value widths, keys with or without the QJL stage
+ * ([3BITS] "Python + HuggingFace": a cache object built with key_bits and value_bits, and a
+ * stage-1 quantizer alone returning indices and norms; the same page notes that the llama.cpp
+ * forks switch QJL off for keys).  key_bits counts every stored bit of a key coordinate: with
+ * qjl != 0 the key book has 2^(key_bits-1) levels plus one sign bit per projected coordinate
+ * (m = d); with qjl == 0 it has 2^key_bits levels and the page has no sign and gamma regions.
+ * value_bits: value book of 2^value_bits levels.  The page holds the version-1 regions in the
+ * same order and bit order with KB = key_bits - (qjl ? 1 : 0) key planes, VB = value_bits value
+ * planes and, without QJL, regions 2 (signs) and 4 (gamma) dropped:
+ *   page bytes = P (KB d/8 + 4 + VB d/8 + 4) + (qjl ? P (d/8 + 4) : 0).
+ * qjl != 0 with key_bits == value_bits is version 1 (tq_ctx_create(d, key_bits, d, ...)).
+ * Version-2 contexts quantize, decode (TQ_DECODE_AUTO or _SIMT only) and dequantize on CUDA
+ * cores.  TQ_EUNSUPPORTED unless d in {64,128,256}, 1 <= KB <= 5 and 1 <= value_bits <= 5. */
+int tq_ctx_create_kv(int d, int key_bits, int value_bits, int qjl, uint64_t seed, int device, tq_ctx** out);
 void tq_ctx_destroy(tq_ctx* ctx);
 
 /* Bytes of one page, and of a whole cache [batch][kv_heads][ceil(max_tokens/P)] pages

@@ -43,6 +43,7 @@ _SIGS = {
     "tq_make_rotation": (_c_int, [_c_int, ctypes.c_uint64, _dp]),
     "tq_make_projection": (_c_int, [_c_int, _c_int, ctypes.c_uint64, _dp]),
     "tq_ctx_create": (_c_int, [_c_int, _c_int, _c_int, ctypes.c_uint64, _c_int, ctypes.POINTER(_vp)]),
+    "tq_ctx_create_kv": (_c_int, [_c_int, _c_int, _c_int, _c_int, ctypes.c_uint64, _c_int, ctypes.POINTER(_vp)]),
     "tq_ctx_destroy": (None, [_vp]),
     "tq_page_bytes": (_c_size, [_vp]),
     "tq_cache_bytes": (_c_size, [_vp, _c_int, _c_int, _c_int]),
@@ -146,6 +147,13 @@ def tq_ctx_create(d, bits, m, seed, device):
     return out
 
 
+def tq_ctx_create_kv(d, key_bits, value_bits, qjl, seed, device):
+    out = ctypes.c_void_p()
+    _check("tq_ctx_create_kv", lib().tq_ctx_create_kv(d, key_bits, value_bits, 1 if qjl else 0, ctypes.c_uint64(seed),
+                                                      device, ctypes.byref(out)))
+    return out
+
+
 def tq_ctx_destroy(ctx):
     lib().tq_ctx_destroy(ctx)
 
@@ -200,11 +208,20 @@ def tq_ctx_get_constants(ctx, d, bits, m):
 
 class Context:
     """One (d, bits, m, seed) context on one CUDA device; wraps the C-ABI calls for torch
-    tensors.  Every method is asynchronous on the given (or current) stream."""
+    tensors.  Every method is asynchronous on the given (or current) stream.  With key_bits
+    (and value_bits, qjl) the context has separate key and value widths (format version 2,
+    tq_ctx_create_kv); bits is then ignored."""
 
-    def __init__(self, d, bits, m=None, seed=0, device=0, decode_path="auto"):
-        self.d, self.bits, self.m, self.seed, self.device = d, bits, d if m is None else m, seed, device
-        self._ctx = tq_ctx_create(d, bits, self.m, seed, device)
+    def __init__(self, d, bits=None, m=None, seed=0, device=0, decode_path="auto", key_bits=None,
+                 value_bits=None, qjl=True):
+        self.d, self.seed, self.device = d, seed, device
+        if key_bits is not None:
+            self.key_bits, self.value_bits, self.qjl = key_bits, value_bits, bool(qjl)
+            self.bits, self.m = None, d if qjl else 0
+            self._ctx = tq_ctx_create_kv(d, key_bits, value_bits, qjl, seed, device)
+        else:
+            self.bits, self.m = bits, d if m is None else m
+            self._ctx = tq_ctx_create(d, bits, self.m, seed, device)
         if decode_path != "auto":
             self.set_decode_path(decode_path)
 

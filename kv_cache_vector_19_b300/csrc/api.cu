@@ -22,6 +22,8 @@ bool supported(int d, int bits, int m) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int upload(const std::vector<double>& src, float** dst) {
+  *dst = nullptr;
+  if (src.empty()) return TQ_OK;   // e.g. S for keys without QJL (m = 0)
   std::vector<float> f(src.size());
   for (size_t i = 0; i < src.size(); ++i) f[i] = (float)src[i];
   if (cudaMalloc(reinterpret_cast<void**>(dst), f.size() * sizeof(float)) != cudaSuccess) return TQ_ENOMEM;
@@ -90,8 +92,8 @@ std::vector<float> exact_tables(const tq_ctx* c, const std::vector<double>& sp) 
     }
   };
   split(c->pi.data(), dd, 0, dd);
-  split(c->s.data(), dd, 2 * dd, 3 * dd);
-  split(sp.data(), dd, 4 * dd, 5 * dd);
+  split(c->s.data(), c->s.size(), 2 * dd, 3 * dd);   // m x d (empty without QJL)
+  split(sp.data(), sp.size(), 4 * dd, 5 * dd);
   const size_t b = 6 * dd;
   split(c->tk.data(), c->tk.size(), b, b + 32);
   split(c->tv.data(), c->tv.size(), b + 64, b + 96);
@@ -130,20 +132,23 @@ struct DeviceGuard {
 
 }  // namespace
 
-extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, tq_ctx** out) {
-  if (!out) return TQ_EINVAL;
-  *out = nullptr;
-  if (!supported(d, bits, m)) return TQ_EUNSUPPORTED;
+namespace {
+// A context of format version 1 (bits > 0: kb = bits - 1 key planes, vb = bits value planes,
+// m = d) or version 2 (bits = 0: any kb, vb in [1, 5], m = d or 0).
+int create(int d, int bits, int kb, int vb, int m, uint64_t seed, int device, tq_ctx** out) {
   tq_ctx* c = new (std::nothrow) tq_ctx();
   if (!c) return TQ_ENOMEM;
   c->d = d;
   c->bits = bits;
+  c->kb = kb;
+  c->vb = vb;
   c->m = m;
   c->seed = seed;
   c->device = device;
-  c->lk = 1 << (bits - 1);
-  c->lv = 1 << bits;
-  c->page_bytes = tq::page_bytes(d, bits, m);
+  c->lk = 1 << kb;
+  c->lv = 1 << vb;
+  c->page_bytes = (size_t)TQ_PAGE_TOKENS * ((size_t)kb * d / 8 + 4 + (size_t)vb * d / 8 + 4) +
+                  (m > 0 ? (size_t)TQ_PAGE_TOKENS * ((size_t)m / 8 + 4) : 0);
   c->pi.resize((size_t)d * d);
   c->s.resize((size_t)m * d);
   c->ck.resize(c->lk);
@@ -181,7 +186,7 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
     if (rc == TQ_OK) rc = upload(c->tk, &c->d_tk);
     if (rc == TQ_OK) rc = upload(c->cv, &c->d_cv);
     if (rc == TQ_OK) rc = upload(c->tv, &c->d_tv);
-    if (rc == TQ_OK) {
+    if (rc == TQ_OK && bits > 0) {
       std::vector<double> ak = plane_alphas(c->ck, bits - 1), av = plane_alphas(c->cv, bits);
       for (double x : ak) c->asum_k += (float)x;
       for (double x : av) c->asum_v += (float)x;
@@ -190,10 +195,14 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
     }
     if (rc == TQ_OK && cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
       rc = TQ_ECUDA;
-    if (rc == TQ_OK) rc = prepare_quantize_simt(c);
-    if (rc == TQ_OK) rc = tq::prepare_decode_mma(c);
-    if (rc == TQ_OK) rc = tq::prepare_decode_tc(c);
-    if (rc == TQ_OK) rc = tq::prepare_decode_f4(c);
+    if (bits == 0) {
+      if (rc == TQ_OK) rc = tq::prepare_kv2(c);
+    } else {
+      if (rc == TQ_OK) rc = prepare_quantize_simt(c);
+      if (rc == TQ_OK) rc = tq::prepare_decode_mma(c);
+      if (rc == TQ_OK) rc = tq::prepare_decode_tc(c);
+      if (rc == TQ_OK) rc = tq::prepare_decode_f4(c);
+    }
     std::vector<double> sp((size_t)m * d);   // S'[i][j] row-major
     for (int i = 0; i < m; ++i)
       for (int j = 0; j < d; ++j) sp[(size_t)i * d + j] = spt[(size_t)j * m + i];
@@ -203,7 +212,7 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
           cudaMemcpy(c->d_exact, et.data(), et.size() * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess)
         rc = TQ_ENOMEM;
     }
-    if (rc == TQ_OK && d == 128) {
+    if (rc == TQ_OK && d == 128 && bits > 0) {
       std::vector<uint8_t> blob = quantizer_blob(c->pi, sp);
       if (cudaMalloc(reinterpret_cast<void**>(&c->d_qblob), blob.size()) != cudaSuccess ||
           cudaMemcpy(c->d_qblob, blob.data(), blob.size(), cudaMemcpyHostToDevice) != cudaSuccess)
@@ -224,6 +233,26 @@ extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, 
   tq::noalloc_forget_device(device);
   *out = c;
   return TQ_OK;
+}
+}  // namespace
+
+extern "C" int tq_ctx_create(int d, int bits, int m, uint64_t seed, int device, tq_ctx** out) {
+  if (!out) return TQ_EINVAL;
+  *out = nullptr;
+  if (!supported(d, bits, m)) return TQ_EUNSUPPORTED;
+  return create(d, bits, bits - 1, bits, m, seed, device, out);
+}
+
+extern "C" int tq_ctx_create_kv(int d, int key_bits, int value_bits, int qjl, uint64_t seed, int device,
+                                tq_ctx** out) {
+  if (!out) return TQ_EINVAL;
+  *out = nullptr;
+  if (d != 64 && d != 128 && d != 256) return TQ_EUNSUPPORTED;
+  const int kb = qjl ? key_bits - 1 : key_bits;
+  if (kb < 1 || kb > 5 || value_bits < 1 || value_bits > 5) return TQ_EUNSUPPORTED;
+  if (qjl && key_bits == value_bits)   // the version-1 format, with its tensor-core kernels
+    return create(d, key_bits, kb, value_bits, d, seed, device, out);
+  return create(d, 0, kb, value_bits, qjl ? d : 0, seed, device, out);
 }
 
 extern "C" void tq_ctx_destroy(tq_ctx* ctx) { release(ctx); }
@@ -262,6 +291,8 @@ extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, i
   if (!k || !v || !start_pos || !cache) return TQ_EINVAL;
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(cache, 256) || !aligned(start_pos, 4)) return TQ_EINVAL;
   DeviceGuard guard(ctx->device);
+  if (ctx->bits == 0)
+    return tq::launch_quantize_kv2(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
   if (n_tokens <= tq::kFewTokens)
     return tq::launch_quantize_few(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
   if (ctx->d == 128)
@@ -276,7 +307,7 @@ extern "C" int tq_ctx_set_decode_path(tq_ctx* ctx, int path) {
     case TQ_DECODE_SIMT:
       break;
     case TQ_DECODE_MMA:
-      if (ctx->d != 64 && ctx->d != 128 && ctx->d != 256) return TQ_EUNSUPPORTED;
+      if (ctx->bits == 0 || (ctx->d != 64 && ctx->d != 128 && ctx->d != 256)) return TQ_EUNSUPPORTED;
       break;
     case TQ_DECODE_TC:
     case TQ_DECODE_TC4:
@@ -377,6 +408,9 @@ extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int 
   if (kern == TQ_DECODE_MMA)
     return tq::launch_decode_mma(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
                                  workspace, stream);
+  if (ctx->bits == 0)
+    return tq::launch_decode_kv2(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
+                                 workspace, stream);
   return launch_decode_simt(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
                             workspace, stream);
 }
@@ -390,6 +424,9 @@ extern "C" int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch,
   if (!cache || !start_pos || !aligned(cache, 256) || !aligned(start_pos, 4)) return TQ_EINVAL;
   if ((k_out && !aligned(k_out, 4)) || (v_out && !aligned(v_out, 4))) return TQ_EINVAL;
   DeviceGuard guard(ctx->device);
+  if (ctx->bits == 0)
+    return tq::launch_dequantize_kv2(ctx, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out,
+                                     stream);
   return tq::launch_dequantize(ctx, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, stream);
 }
 

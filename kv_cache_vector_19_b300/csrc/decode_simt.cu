@@ -322,6 +322,14 @@ int launch_d(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_hea
 
 }  // namespace
 
+void launch_combine(const tq_ctx* c, const float* part, float* out, int batch, int q_heads, int splits,
+                    cudaStream_t st) {
+  dim3 grid(q_heads, batch);
+  if (c->d == 64) combine_kernel<64><<<grid, 64, 0, st>>>(part, c->d_pi, out, q_heads, splits);
+  if (c->d == 128) combine_kernel<128><<<grid, 128, 0, st>>>(part, c->d_pi, out, q_heads, splits);
+  if (c->d == 256) combine_kernel<256><<<grid, 256, 0, st>>>(part, c->d_pi, out, q_heads, splits);
+}
+
 void launch_prologue(const tq_ctx* c, const float* q, int batch, int q_heads, float* qr, float* qs,
                      cudaStream_t st) {
   dim3 grid(q_heads, batch);

@@ -40,7 +40,8 @@ struct MmaPlan {
 }  // namespace tq
 
 struct tq_ctx {
-  int d, bits, m, device;
+  int d, bits, m, device;   // bits = 0: format version 2 (kb, vb and m free; m = 0 without QJL)
+  int kb = 0, vb = 0;       // key and value code planes
   uint64_t seed;
   int lk, lv;
   size_t page_bytes;
@@ -125,6 +126,19 @@ void noalloc_forget_device(int device);
 // q~ = Pi q and q_s = S q for every (batch, query head), fp32.
 void launch_prologue(const tq_ctx* c, const float* q, int batch, int q_heads, float* qr, float* qs,
                      cudaStream_t st);
+// Split merge and Pi^T of the CUDA-core decode: out = Pi^T o~ / l per (query head, batch).
+void launch_combine(const tq_ctx* c, const float* part, float* out, int batch, int q_heads, int splits,
+                    cudaStream_t st);
+// Format version 2 (kv2.cu): CUDA-core quantizer, split decode and dequantizer with the plane
+// counts and m read from the context.
+int prepare_kv2(const tq_ctx* c);
+int launch_quantize_kv2(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
+                        const int32_t* start_pos, void* cache, int max_tokens, void* stream);
+int launch_decode_kv2(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
+                      const int32_t* seq_lens, int max_tokens, float* out, float* logits_out, void* workspace,
+                      void* stream);
+int launch_dequantize_kv2(const tq_ctx* c, const void* cache, int batch, int kv_heads, int max_tokens,
+                          const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream);
 }  // namespace tq
 
 int launch_decode_simt(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
