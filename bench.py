@@ -504,7 +504,9 @@ def run_sweep(args):
 def run_case(args, w):
     """One kernel of the workload, alone, at a reduced prefill length: the cases the ncu
     summaries under profiles/ are taken on.  --kernel-case quantize runs tq_quantize_kv of the
-    prefill; decode runs tq_attn_decode over it.  warmup + steps calls, no JSON line."""
+    prefill; decode runs tq_attn_decode over it; scan runs tq_ip_topk (top --topk keys per query
+    head) over it.  warmup + steps calls; prints the mean device time of the timed calls (CUDA
+    events on the launching stream), no JSON line."""
     import torch
 
     import kv_cache_vector_19_b300 as tq
@@ -517,24 +519,45 @@ def run_case(args, w):
     cache = ctx.alloc_cache(B, H, T)
     k, v = data["k"].cuda(), data["v"].cuda()
     zero = torch.zeros(B, dtype=torch.int32, device="cuda")
-    calls = args.warmup + args.steps
+    stream = torch.cuda.current_stream()
     if args.kernel_case == "quantize":
-        for _ in range(calls):
+        def call():
             ctx.quantize_kv(k, v, zero, cache, T)
     else:
         ctx.quantize_kv(k, v, zero, cache, T)
-        ws = ctx.alloc_workspace(B, Hq, H, T)
         q = data["q"][0].cuda().contiguous()
-        out = torch.empty_like(q)
         lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
-        for _ in range(calls):
-            ctx.attn_decode(q, cache, lens, H, T, out, ws)
+        if args.kernel_case == "decode":
+            ws = ctx.alloc_workspace(B, Hq, H, T)
+            out = torch.empty_like(q)
+
+            def call():
+                ctx.attn_decode(q, cache, lens, H, T, out, ws)
+        else:
+            kk = args.topk
+            ws = ctx.alloc_topk_workspace(B, Hq, H, T)
+            oi = torch.empty(B, Hq, kk, dtype=torch.int32, device="cuda")
+            osc = torch.empty(B, Hq, kk, dtype=torch.float32, device="cuda")
+
+            def call():
+                ctx.ip_topk(q, cache, lens, H, T, kk, out_idx=oi, out_score=osc, workspace=ws)
+    for _ in range(args.warmup):
+        call()
     torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / max(args.steps, 1)
     st = ctx.device_status()
+    cache_mb = cache.numel() * cache.element_size() / 1e6
     ctx.close()
     if st != tq.TQ_OK:
         raise SystemExit(f"device status: {tq.tq_status_string(st)}")
-    print(f"{args.kernel_case} case: {w.name}, {T} tokens, {calls} calls, status ok", flush=True)
+    print(f"{args.kernel_case} case: {w.name}, {T} tokens, {args.warmup + args.steps} calls, status ok, "
+          f"{ms * 1e3:.1f} us per call (back to back, cache {cache_mb:.0f} MB)", flush=True)
     return 0
 
 
@@ -547,9 +570,10 @@ def main():
     ap.add_argument("--workload", default="longctx", choices=["longctx", "llama8b", "llama70b", "tiny"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-case", choices=["quantize", "decode"], default=None,
+    ap.add_argument("--kernel-case", choices=["quantize", "decode", "scan"], default=None,
                     help="run one kernel of the workload alone (profiling case), no JSON line")
     ap.add_argument("--tokens", type=int, default=0, help="prefill length of --kernel-case (default: workload's)")
+    ap.add_argument("--topk", type=int, default=100, help="k of --kernel-case scan")
     args = ap.parse_args()
     if args.warmup < 3 and not args.sweep:
         args.warmup = 3

@@ -214,6 +214,25 @@ int tq_attn_decode_noalloc(const tq_ctx* ctx, const float* q, int batch, int q_h
                            const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
                            float* logits_out, void* stream);
 
+/* Compressed inner-product scan: for every query head, the k cached keys of its KV head with
+ * the largest estimated inner product ([BLOG] 6.4, research directions: vector search and the
+ * compression of RAG indexes; its FAQ: the method applies to any high-dimensional vectors):
+ *   <q, k^_t> = n_t <Pi q, c_K[idx_t]> + gamma_t sqrt(pi/2)/m <S q, 2 sigma_t - 1>
+ * (the QJL term only when the keys keep it), i.e. the decode score times sqrt(d).
+ *   q, cache, seq_lens, batch, q_heads, kv_heads, max_tokens  as tq_attn_decode (the scores
+ *              come from the decode kernel that serves the context)
+ *   k          1 .. TQ_TOPK_MAX
+ *   out_idx    device int32 [batch][q_heads][k]: slots, by decreasing estimate (the fp32 value
+ *              out_score returns), equal estimates by increasing slot; -1 past seq_lens[b]
+ *   out_score  device fp32 [batch][q_heads][k]: the estimates (-inf past seq_lens[b])
+ *   workspace  device, 256-byte aligned, >= tq_ip_topk_workspace_bytes(...) bytes
+ * Errors: tq_attn_decode's, TQ_EINVAL for k or the outputs, TQ_ENOMEM for a short workspace. */
+#define TQ_TOPK_MAX 1024
+size_t tq_ip_topk_workspace_bytes(const tq_ctx* ctx, int batch, int q_heads, int kv_heads, int max_tokens);
+int tq_ip_topk(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
+               const int32_t* seq_lens, int max_tokens, int k, int32_t* out_idx, float* out_score, void* workspace,
+               size_t workspace_bytes, void* stream);
+
 /* Reconstructs cached vectors in the original frame, from the page contents alone
  * ([BLOG] 1.2: dequantization of stage 1, x~ = n Pi^T c[idx], and the stage-2 estimate of the
  * key residual from its signs; [3BITS] "Python + HuggingFace": dequantize(indices, norms)):

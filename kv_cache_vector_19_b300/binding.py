@@ -23,6 +23,7 @@ TQ_EBOUNDS = -5
 TQ_ENOMEM = -6
 TQ_ENOTCONV = -7
 TQ_ESCRATCH = -8
+TQ_TOPK_MAX = 1024
 TQ_DECODE_AUTO, TQ_DECODE_SIMT, TQ_DECODE_MMA, TQ_DECODE_TC, TQ_DECODE_TC4 = 0, 1, 2, 3, 4
 DECODE_PATHS = {"auto": TQ_DECODE_AUTO, "simt": TQ_DECODE_SIMT, "mma": TQ_DECODE_MMA, "tc": TQ_DECODE_TC,
                 "tc4": TQ_DECODE_TC4}
@@ -55,6 +56,9 @@ _SIGS = {
                                 _c_size, _vp]),
     "tq_attn_decode_noalloc": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp]),
     "tq_dequantize_kv": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp]),
+    "tq_ip_topk_workspace_bytes": (_c_size, [_vp, _c_int, _c_int, _c_int, _c_int]),
+    "tq_ip_topk": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_size,
+                            _vp]),
     "tq_selftest_bounded_wait": (_c_int, [_vp, _vp]),
     "tq_get_device_status": (_c_int, [_vp, _vp]),
     "tq_status_string": (ctypes.c_char_p, [_c_int]),
@@ -292,6 +296,33 @@ class Context:
                             _ptr(out), _ptr(logits), _ptr(workspace), workspace.numel() * workspace.element_size(),
                             _stream_handle(stream))
         _check("tq_attn_decode", rc)
+
+    def alloc_topk_workspace(self, batch, q_heads, kv_heads, max_tokens, device="cuda"):
+        """Device scratch of tq_ip_topk (tq_ip_topk_workspace_bytes bytes)."""
+        import torch
+        n = lib().tq_ip_topk_workspace_bytes(self._ctx, batch, q_heads, kv_heads, max_tokens)
+        if n == 0:
+            raise TQError("tq_ip_topk_workspace_bytes", TQ_EINVAL)
+        return torch.empty(n, dtype=torch.uint8, device=device)
+
+    def ip_topk(self, q, cache, seq_lens, kv_heads, max_tokens, k, out_idx=None, out_score=None, workspace=None,
+                stream=None):
+        """Compressed inner-product scan (tq_ip_topk): per query head the k slots with the largest
+        estimated <q, k^_t>.  q: fp32 [B, Hq, d]; seq_lens: int32 [B] on the device.  Returns
+        (out_idx int32 [B, Hq, k], out_score fp32 [B, Hq, k])."""
+        import torch
+        B, Hq, d = q.shape
+        if out_idx is None:
+            out_idx = torch.empty(B, Hq, k, dtype=torch.int32, device=q.device)
+        if out_score is None:
+            out_score = torch.empty(B, Hq, k, dtype=torch.float32, device=q.device)
+        if workspace is None:
+            workspace = self.alloc_topk_workspace(B, Hq, kv_heads, max_tokens)
+        rc = lib().tq_ip_topk(self._ctx, _ptr(q), B, Hq, kv_heads, _ptr(cache), _ptr(seq_lens), max_tokens, k,
+                              _ptr(out_idx), _ptr(out_score), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        _check("tq_ip_topk", rc)
+        return out_idx, out_score
 
     def device_status(self, stream=None):
         """Synchronises the stream; returns (and clears) the sticky device status code."""

@@ -415,6 +415,42 @@ extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int 
                             workspace, stream);
 }
 
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+}  // namespace
+
+extern "C" size_t tq_ip_topk_workspace_bytes(const tq_ctx* ctx, int batch, int q_heads, int kv_heads,
+                                             int max_tokens) {
+  const size_t dw = tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens);
+  if (dw == 0) return 0;
+  const size_t rows = (size_t)batch * q_heads;
+  return align256(dw) + align256(rows * (size_t)max_tokens * 4) + align256(rows * (size_t)ctx->d * 4);
+}
+
+extern "C" int tq_ip_topk(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                          const void* cache, const int32_t* seq_lens, int max_tokens, int k, int32_t* out_idx,
+                          float* out_score, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ctx || k < 1 || k > TQ_TOPK_MAX || !out_idx || !out_score || !aligned(out_idx, 4) || !aligned(out_score, 4))
+    return TQ_EINVAL;
+  // the decode's own checks (out stands in for the decode output, which lives in the workspace)
+  const int rc0 = tq::check_decode_args(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out_score,
+                                        nullptr);
+  if (rc0 != TQ_OK) return rc0;
+  if (!workspace || !aligned(workspace, 256)) return TQ_EINVAL;
+  const size_t need = tq_ip_topk_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens);
+  if (need == 0) return TQ_EINVAL;
+  if (workspace_bytes < need) return TQ_ENOMEM;
+  const size_t dw = tq_decode_workspace_bytes(ctx, batch, q_heads, kv_heads, max_tokens);
+  const size_t rows = (size_t)batch * q_heads;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  float* lg = reinterpret_cast<float*>(w + align256(dw));
+  float* o = reinterpret_cast<float*>(w + align256(dw) + align256(rows * (size_t)max_tokens * 4));
+  const int rc = tq_attn_decode(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, o, lg, w, dw, stream);
+  if (rc != TQ_OK) return rc;
+  DeviceGuard guard(ctx->device);
+  return tq::launch_topk(ctx, lg, seq_lens, batch, q_heads, max_tokens, k, out_idx, out_score, stream);
+}
+
 extern "C" int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch, int kv_heads, int max_tokens,
                                 const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream) {
   if (!ctx) return TQ_EINVAL;

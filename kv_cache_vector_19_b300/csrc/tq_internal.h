@@ -129,6 +129,9 @@ void launch_prologue(const tq_ctx* c, const float* q, int batch, int q_heads, fl
 // Split merge and Pi^T of the CUDA-core decode: out = Pi^T o~ / l per (query head, batch).
 void launch_combine(const tq_ctx* c, const float* part, float* out, int batch, int q_heads, int splits,
                     cudaStream_t st);
+// Top k of each (batch, query head) row of decode logits (scan.cu), scaled back by sqrt(d).
+int launch_topk(const tq_ctx* c, const float* logits, const int32_t* seq_lens, int batch, int q_heads,
+                int max_tokens, int k, int32_t* out_idx, float* out_score, void* stream);
 // Format version 2 (kv2.cu): CUDA-core quantizer, split decode and dequantizer with the plane
 // counts and m read from the context.
 int prepare_kv2(const tq_ctx* c);
