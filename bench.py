@@ -516,24 +516,42 @@ def run_case(args, w):
     data = workloads.generate(wl)
     B, H, Hq, T, d = wl.batch, wl.kv_heads, wl.q_heads, wl.tokens, wl.d
     ctx = tq.Context(d, wl.b, seed=wl.seed)
-    cache = ctx.alloc_cache(B, H, T)
     k, v = data["k"].cuda(), data["v"].cuda()
     zero = torch.zeros(B, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
-    if args.kernel_case == "quantize":
-        def call():
-            ctx.quantize_kv(k, v, zero, cache, T)
+    if args.paged:   # a pool of blocks in a seeded random order, one table row per sequence
+        max_blocks = (T + 127) // 128
+        n_blocks = B * max_blocks
+        perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(wl.seed + 1))
+        table = perm.to(torch.int32).reshape(B, max_blocks).cuda()
+        cache = ctx.alloc_pool(H, n_blocks)
+        T = 128 * max_blocks
+
+        def quantize():
+            ctx.quantize_kv_paged(k, v, zero, cache, n_blocks, table)
     else:
-        ctx.quantize_kv(k, v, zero, cache, T)
+        cache = ctx.alloc_cache(B, H, T)
+
+        def quantize():
+            ctx.quantize_kv(k, v, zero, cache, T)
+    if args.kernel_case == "quantize":
+        call = quantize
+    else:
+        quantize()
         q = data["q"][0].cuda().contiguous()
-        lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        lens = torch.full((B,), wl.tokens, dtype=torch.int32, device="cuda")
         if args.kernel_case == "decode":
             ws = ctx.alloc_workspace(B, Hq, H, T)
             out = torch.empty_like(q)
-
-            def call():
-                ctx.attn_decode(q, cache, lens, H, T, out, ws)
+            if args.paged:
+                def call():
+                    ctx.attn_decode_paged(q, cache, n_blocks, table, lens, H, out, ws)
+            else:
+                def call():
+                    ctx.attn_decode(q, cache, lens, H, T, out, ws)
         else:
+            if args.paged:
+                raise SystemExit("--paged applies to the quantize and decode cases")
             kk = args.topk
             ws = ctx.alloc_topk_workspace(B, Hq, H, T)
             oi = torch.empty(B, Hq, kk, dtype=torch.int32, device="cuda")
@@ -556,7 +574,8 @@ def run_case(args, w):
     ctx.close()
     if st != tq.TQ_OK:
         raise SystemExit(f"device status: {tq.tq_status_string(st)}")
-    print(f"{args.kernel_case} case: {w.name}, {T} tokens, {args.warmup + args.steps} calls, status ok, "
+    print(f"{args.kernel_case} case{' (paged pool)' if args.paged else ''}: {w.name}, {wl.tokens} tokens, "
+          f"{args.warmup + args.steps} calls, status ok, "
           f"{ms * 1e3:.1f} us per call (back to back, cache {cache_mb:.0f} MB)", flush=True)
     return 0
 
@@ -574,6 +593,8 @@ def main():
                     help="run one kernel of the workload alone (profiling case), no JSON line")
     ap.add_argument("--tokens", type=int, default=0, help="prefill length of --kernel-case (default: workload's)")
     ap.add_argument("--topk", type=int, default=100, help="k of --kernel-case scan")
+    ap.add_argument("--paged", action="store_true",
+                    help="--kernel-case quantize / decode on a block pool through a shuffled block table")
     args = ap.parse_args()
     if args.warmup < 3 and not args.sweep:
         args.warmup = 3

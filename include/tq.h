@@ -247,6 +247,39 @@ int tq_ip_topk(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv
 int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch, int kv_heads, int max_tokens,
                      const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream);
 
+/* Paged (block-table) cache: the compressed pages live in a pool of blocks that sequences
+ * borrow in any order, the layout of a PagedAttention-style serving engine ([BLOG] 3.5 "Другие
+ * инструменты и фреймворки", vLLM: PagedAttention; [3BITS] "vLLM": the TurboQuant attention
+ * backend behind --kv-cache-dtype).  The arithmetic, the page format and every kernel are
+ * those of the contiguous calls; only where a page lives differs.
+ *   pool         device, 256-byte aligned, tq_paged_pool_bytes(ctx, kv_heads, n_blocks) bytes:
+ *                n_blocks blocks, each the kv_heads pages (tq_page_bytes each) of 128
+ *                consecutive token slots; page (block, h) at byte (block * kv_heads + h) *
+ *                tq_page_bytes.  Untouched bytes are never read by a decode that stays
+ *                within seq_lens.
+ *   block_table  device int32 [batch][max_blocks]: block_table[b][p] = the block holding slots
+ *                128 p .. 128 p + 127 of sequence b.  Entries are read only for pages a call
+ *                touches.  An entry outside [0, n_blocks) is clamped into the pool and sets
+ *                the sticky TQ_EBOUNDS flag; two sequences given the same block share it.
+ *   max_blocks   entries per table row; the sequences' capacity is max_blocks * 128 slots and
+ *                takes the place of max_tokens in every other argument rule (start_pos,
+ *                seq_lens, workspace: tq_decode_workspace_bytes(..., max_blocks * 128)).
+ * Otherwise arguments, errors and results exactly as tq_quantize_kv, tq_attn_decode and
+ * tq_dequantize_kv with `cache` replaced by (pool, n_blocks, block_table, max_blocks):
+ * a paged pool whose table maps (b, p) to block b * max_blocks + p holds the contiguous
+ * cache byte for byte when kv_heads == 1, and any table gives bit-identical outputs. */
+size_t tq_paged_pool_bytes(const tq_ctx* ctx, int kv_heads, int n_blocks);
+int tq_quantize_kv_paged(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
+                         int n_tokens, const int32_t* start_pos, void* pool, int n_blocks,
+                         const int32_t* block_table, int max_blocks, void* stream);
+int tq_attn_decode_paged(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                         const void* pool, int n_blocks, const int32_t* block_table, int max_blocks,
+                         const int32_t* seq_lens, float* out, float* logits_out, void* workspace,
+                         size_t workspace_bytes, void* stream);
+int tq_dequantize_kv_paged(const tq_ctx* ctx, const void* pool, int n_blocks, const int32_t* block_table,
+                           int max_blocks, int batch, int kv_heads, const int32_t* start_pos, int n_tokens,
+                           float* k_out, float* v_out, void* stream);
+
 /* Self-test of the device-side failure path: launches one thread that waits, with the same
  * bounded wait every kernel uses, on an mbarrier nothing arrives at.  The wait gives up after
  * its limit (2 s), sets the sticky timeout flag and the kernel returns; a following

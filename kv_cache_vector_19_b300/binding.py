@@ -59,6 +59,12 @@ _SIGS = {
     "tq_ip_topk_workspace_bytes": (_c_size, [_vp, _c_int, _c_int, _c_int, _c_int]),
     "tq_ip_topk": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_size,
                             _vp]),
+    "tq_paged_pool_bytes": (_c_size, [_vp, _c_int, _c_int]),
+    "tq_quantize_kv_paged": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp, _c_int, _vp]),
+    "tq_attn_decode_paged": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _c_int, _vp, _vp, _vp,
+                                      _vp, _c_size, _vp]),
+    "tq_dequantize_kv_paged": (_c_int, [_vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp,
+                                        _vp]),
     "tq_selftest_bounded_wait": (_c_int, [_vp, _vp]),
     "tq_get_device_status": (_c_int, [_vp, _vp]),
     "tq_status_string": (ctypes.c_char_p, [_c_int]),
@@ -296,6 +302,37 @@ class Context:
                             _ptr(out), _ptr(logits), _ptr(workspace), workspace.numel() * workspace.element_size(),
                             _stream_handle(stream))
         _check("tq_attn_decode", rc)
+
+    # ---- paged (block-table) cache: pool of blocks, each the kv_heads pages of 128 slots ----
+    def alloc_pool(self, kv_heads, n_blocks):
+        import torch
+        n = lib().tq_paged_pool_bytes(self._ctx, kv_heads, n_blocks)
+        if n == 0:
+            raise TQError("tq_paged_pool_bytes", TQ_EINVAL)
+        return torch.empty(n, dtype=torch.uint8, device=f"cuda:{self.device}")
+
+    def quantize_kv_paged(self, k, v, start_pos, pool, n_blocks, block_table, stream=None):
+        """k, v: bf16 [B, Hkv, n_tokens, d]; block_table: int32 [B, max_blocks] on the device."""
+        B, H, N, d = k.shape
+        rc = lib().tq_quantize_kv_paged(self._ctx, _ptr(k), _ptr(v), B, H, N, _ptr(start_pos), _ptr(pool), n_blocks,
+                                        _ptr(block_table), block_table.shape[1], _stream_handle(stream))
+        _check("tq_quantize_kv_paged", rc)
+
+    def attn_decode_paged(self, q, pool, n_blocks, block_table, seq_lens, kv_heads, out, workspace, logits=None,
+                          stream=None):
+        """As attn_decode, on a block pool; the workspace is that of max_tokens = 128 * max_blocks."""
+        B, Hq, d = q.shape
+        rc = lib().tq_attn_decode_paged(self._ctx, _ptr(q), B, Hq, kv_heads, _ptr(pool), n_blocks, _ptr(block_table),
+                                        block_table.shape[1], _ptr(seq_lens), _ptr(out), _ptr(logits), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        _check("tq_attn_decode_paged", rc)
+
+    def dequantize_kv_paged(self, pool, n_blocks, block_table, start_pos, batch, kv_heads, n_tokens, k_out=None,
+                            v_out=None, stream=None):
+        rc = lib().tq_dequantize_kv_paged(self._ctx, _ptr(pool), n_blocks, _ptr(block_table), block_table.shape[1],
+                                          batch, kv_heads, _ptr(start_pos), n_tokens, _ptr(k_out), _ptr(v_out),
+                                          _stream_handle(stream))
+        _check("tq_dequantize_kv_paged", rc)
 
     def alloc_topk_workspace(self, batch, q_heads, kv_heads, max_tokens, device="cuda"):
         """Device scratch of tq_ip_topk (tq_ip_topk_workspace_bytes bytes)."""

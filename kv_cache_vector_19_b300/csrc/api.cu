@@ -280,9 +280,10 @@ extern "C" int tq_ctx_get_constants(const tq_ctx* ctx, double* pi, double* s, do
   return TQ_OK;
 }
 
-extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
-                              int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
-                              void* stream) {
+namespace {
+
+int quantize_impl(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
+                  const int32_t* start_pos, void* cache, int max_tokens, const tq::PageMap& pm, void* stream) {
   if (!ctx) return TQ_EINVAL;
   if (batch < 1 || kv_heads < 1 || n_tokens < 0 || max_tokens < 1) return TQ_EINVAL;
   if (batch > 65535 || kv_heads > 65535) return TQ_EINVAL;
@@ -292,12 +293,47 @@ extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, i
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(cache, 256) || !aligned(start_pos, 4)) return TQ_EINVAL;
   DeviceGuard guard(ctx->device);
   if (ctx->bits == 0)
-    return tq::launch_quantize_kv2(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
+    return tq::launch_quantize_kv2(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream, pm);
   if (n_tokens <= tq::kFewTokens)
-    return tq::launch_quantize_few(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
+    return tq::launch_quantize_few(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream, pm);
   if (ctx->d == 128)
-    return tq::launch_quantize_tc(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
-  return launch_quantize_simt(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream);
+    return tq::launch_quantize_tc(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream, pm);
+  return launch_quantize_simt(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream, pm);
+}
+
+// The block-table arguments of the paged entry points: TQ_OK and the page map, or TQ_EINVAL.
+int paged_map(const void* pool, int n_blocks, const int32_t* block_table, int max_blocks, tq::PageMap* pm,
+              int* max_tokens) {
+  if (!pool || !block_table || n_blocks < 1 || max_blocks < 1) return TQ_EINVAL;
+  if (max_blocks > INT32_MAX / TQ_PAGE_TOKENS || !aligned(block_table, 4)) return TQ_EINVAL;
+  pm->table = block_table;
+  pm->stride = max_blocks;
+  pm->n_blocks = n_blocks;
+  *max_tokens = max_blocks * TQ_PAGE_TOKENS;
+  return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
+                              int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
+                              void* stream) {
+  return quantize_impl(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, tq::PageMap(), stream);
+}
+
+extern "C" size_t tq_paged_pool_bytes(const tq_ctx* ctx, int kv_heads, int n_blocks) {
+  if (!ctx || kv_heads < 1 || n_blocks < 1) return 0;
+  return (size_t)n_blocks * kv_heads * ctx->page_bytes;
+}
+
+extern "C" int tq_quantize_kv_paged(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
+                                    int n_tokens, const int32_t* start_pos, void* pool, int n_blocks,
+                                    const int32_t* block_table, int max_blocks, void* stream) {
+  tq::PageMap pm;
+  int max_tokens = 0;
+  const int rc = paged_map(pool, n_blocks, block_table, max_blocks, &pm, &max_tokens);
+  if (rc != TQ_OK) return rc;
+  return quantize_impl(ctx, k, v, batch, kv_heads, n_tokens, start_pos, pool, max_tokens, pm, stream);
 }
 
 extern "C" int tq_ctx_set_decode_path(tq_ctx* ctx, int path) {
@@ -389,9 +425,11 @@ int check_decode_args(const tq_ctx* ctx, const float* q, int batch, int q_heads,
 }
 }  // namespace tq
 
-extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
-                              const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
-                              float* logits_out, void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+int decode_impl(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
+                const int32_t* seq_lens, int max_tokens, float* out, float* logits_out, void* workspace,
+                size_t workspace_bytes, const tq::PageMap& pm, void* stream) {
   const int rc = tq::check_decode_args(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out);
   if (rc != TQ_OK) return rc;
   if (!workspace || !aligned(workspace, 256)) return TQ_EINVAL;
@@ -401,18 +439,39 @@ extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int 
   DeviceGuard guard(ctx->device);
   if (kern == TQ_DECODE_TC4)
     return tq::launch_decode_f4(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
-                                workspace, stream);
+                                workspace, stream, pm);
   if (kern == TQ_DECODE_TC)
     return tq::launch_decode_tc(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
-                                workspace, stream);
+                                workspace, stream, pm);
   if (kern == TQ_DECODE_MMA)
     return tq::launch_decode_mma(ctx, mp, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
-                                 workspace, stream);
+                                 workspace, stream, pm);
   if (ctx->bits == 0)
     return tq::launch_decode_kv2(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
-                                 workspace, stream);
+                                 workspace, stream, pm);
   return launch_decode_simt(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out,
-                            workspace, stream);
+                            workspace, stream, pm);
+}
+
+}  // namespace
+
+extern "C" int tq_attn_decode(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                              const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
+                              float* logits_out, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out, workspace,
+                     workspace_bytes, tq::PageMap(), stream);
+}
+
+extern "C" int tq_attn_decode_paged(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                                    const void* pool, int n_blocks, const int32_t* block_table, int max_blocks,
+                                    const int32_t* seq_lens, float* out, float* logits_out, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  tq::PageMap pm;
+  int max_tokens = 0;
+  const int rc = paged_map(pool, n_blocks, block_table, max_blocks, &pm, &max_tokens);
+  if (rc != TQ_OK) return rc;
+  return decode_impl(ctx, q, batch, q_heads, kv_heads, pool, seq_lens, max_tokens, out, logits_out, workspace,
+                     workspace_bytes, pm, stream);
 }
 
 namespace {
@@ -451,8 +510,11 @@ extern "C" int tq_ip_topk(const tq_ctx* ctx, const float* q, int batch, int q_he
   return tq::launch_topk(ctx, lg, seq_lens, batch, q_heads, max_tokens, k, out_idx, out_score, stream);
 }
 
-extern "C" int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch, int kv_heads, int max_tokens,
-                                const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream) {
+namespace {
+
+int dequantize_impl(const tq_ctx* ctx, const void* cache, int batch, int kv_heads, int max_tokens,
+                    const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, const tq::PageMap& pm,
+                    void* stream) {
   if (!ctx) return TQ_EINVAL;
   if (batch < 1 || kv_heads < 1 || n_tokens < 0 || max_tokens < 1) return TQ_EINVAL;
   if (batch > 65535 || kv_heads > 65535 || n_tokens > max_tokens) return TQ_EINVAL;
@@ -462,8 +524,27 @@ extern "C" int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch,
   DeviceGuard guard(ctx->device);
   if (ctx->bits == 0)
     return tq::launch_dequantize_kv2(ctx, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out,
-                                     stream);
-  return tq::launch_dequantize(ctx, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, stream);
+                                     stream, pm);
+  return tq::launch_dequantize(ctx, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, stream,
+                               pm);
+}
+
+}  // namespace
+
+extern "C" int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch, int kv_heads, int max_tokens,
+                                const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream) {
+  return dequantize_impl(ctx, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, tq::PageMap(),
+                         stream);
+}
+
+extern "C" int tq_dequantize_kv_paged(const tq_ctx* ctx, const void* pool, int n_blocks, const int32_t* block_table,
+                                      int max_blocks, int batch, int kv_heads, const int32_t* start_pos,
+                                      int n_tokens, float* k_out, float* v_out, void* stream) {
+  tq::PageMap pm;
+  int max_tokens = 0;
+  const int rc = paged_map(pool, n_blocks, block_table, max_blocks, &pm, &max_tokens);
+  if (rc != TQ_OK) return rc;
+  return dequantize_impl(ctx, pool, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, pm, stream);
 }
 
 extern "C" int tq_selftest_bounded_wait(const tq_ctx* ctx, void* stream) {

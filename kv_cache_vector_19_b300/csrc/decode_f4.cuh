@@ -87,6 +87,7 @@ __host__ __device__ constexpr int token_sets(int gp) { return gp >= 8 ? 4 : (gp 
 constexpr int kL2Ahead = 12;  // pages prefetched into L2 beyond the shared-memory ring
 constexpr int kRingMax = 8;   // ring slots (as many as fit, at most this; a streaming probe
                               // of this grid runs the whole cache through 4-8 slots at ~5 TB/s)
+static_assert(kRingMax + kL2Ahead <= 32, "a paged segment's ring and L2 look-ahead fit two 32-page windows");
 // Lazy-maximum threshold (natural-log units): a page rescales the running maximum only when
 // one of its logits exceeds it by kTau or a value norm exceeds n_ref, so a weight
 // x = p n_v / n_ref stays below e^0.69 = 1.994 and Y = round(2^15 x) fits 16 bits.  The
@@ -201,8 +202,8 @@ __device__ __forceinline__ float piece_scale(float m) {
   return s;
 }
 
-template <int BITS, int GP>
-__global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Params a) {
+template <int BITS, int GP, bool PAGED>
+__global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Params a, PageMap pm) {
   using C = Cfg<BITS, GP>;
   using PL = typename C::PL;
   constexpr int D = 128, NS = C::NS, PK = C::PK, PV = C::PV, BK = C::BK, BV = C::BV, NBUF = C::NBUF;
@@ -322,19 +323,63 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
     auto ring_slot = [&](int p) { return (pg_base + p) % NBUF; };
     auto ring_use = [&](int p) { return (pg_base + p) / NBUF; };
     auto pg_ptr = [&](int p) { return s_pages + ring_slot(p) * C::PAGE; };
+    // Block pool (PAGED, its own instantiation): the value-waiter warp, which fills the ring,
+    // holds the block ids of the segment's pages [32 win, 32 win + 64), one of each window per
+    // lane, loaded a window ahead, so that a page address is a shuffle, not a dependent load.
+    [[maybe_unused]] const int32_t* trow = nullptr;
+    [[maybe_unused]] int win = 0;
+    [[maybe_unused]] int32_t blk_a = 0, blk_b = 0;
+    auto page_at = [&](int i) -> const uint8_t* {   // page p_lo + i; warp-wide when PAGED
+      if constexpr (PAGED) {
+        const int32_t x = __shfl_sync(0xffffffffu, blk_a, i & 31);
+        const int32_t y = __shfl_sync(0xffffffffu, blk_b, i & 31);
+        int blk = i < 32 * (win + 1) ? x : y;
+        if ((unsigned)blk >= (unsigned)pm.n_blocks) {   // clamped into the pool, reported
+          if (lane == 0) atomicOr(a.status, kFlagBounds);
+          blk = blk < 0 ? 0 : pm.n_blocks - 1;
+        }
+        return a.cache + ((size_t)blk * a.kv_heads + kvh) * PL::bytes;
+      } else {
+        return seq_base + (size_t)(p_lo + i) * PL::bytes;
+      }
+    };
 
     __syncthreads();   // previous segment fully done
-    if (warp == kWarpWV && lane == 0) {
-      const int first = min(n_pages, NBUF);
-      for (int i = 0; i < first; ++i) {
-        const uint32_t si = ring_slot(i);
-        fence_proxy_async();
-        mbar_expect_tx(&s_full[si], PL::bytes);
-        bulk_g2s(s_pages + si * C::PAGE, seq_base + (size_t)(p_lo + i) * PL::bytes, PL::bytes, &s_full[si]);
+    if constexpr (PAGED) {
+      if (warp == kWarpWV) {
+        trow = pm.table + (size_t)b * pm.stride + p_lo;
+        win = 0;
+        blk_a = lane < n_pages ? __ldg(trow + lane) : 0;
+        blk_b = 32 + lane < n_pages ? __ldg(trow + 32 + lane) : 0;
+        const int first = min(n_pages, NBUF);
+        for (int i = 0; i < first; ++i) {
+          const uint8_t* src = page_at(i);
+          if (lane == 0) {
+            const uint32_t si = ring_slot(i);
+            fence_proxy_async();
+            mbar_expect_tx(&s_full[si], PL::bytes);
+            bulk_g2s(s_pages + si * C::PAGE, src, PL::bytes, &s_full[si]);
+          }
+        }
+        if (lane == 0) issued = pg_base + first;
+        for (int i = NBUF; i < min(n_pages, NBUF + kL2Ahead); ++i) {
+          const uint8_t* src = page_at(i);
+          if (lane == 0) prefetch_l2(src, PL::bytes);
+        }
       }
-      issued = pg_base + first;
-      for (int i = NBUF; i < min(n_pages, NBUF + kL2Ahead); ++i)
-        prefetch_l2(seq_base + (size_t)(p_lo + i) * PL::bytes, PL::bytes);
+    } else {
+      if (warp == kWarpWV && lane == 0) {
+        const int first = min(n_pages, NBUF);
+        for (int i = 0; i < first; ++i) {
+          const uint32_t si = ring_slot(i);
+          fence_proxy_async();
+          mbar_expect_tx(&s_full[si], PL::bytes);
+          bulk_g2s(s_pages + si * C::PAGE, page_at(i), PL::bytes, &s_full[si]);
+        }
+        issued = pg_base + first;
+        for (int i = NBUF; i < min(n_pages, NBUF + kL2Ahead); ++i)
+          prefetch_l2(page_at(i), PL::bytes);
+      }
     }
 
     // ---- query operand of this KV head ----
@@ -436,16 +481,39 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
           wait_k(&bv_ready[x], g >> 1);
           group_sync<96>(kNbValue);
           // every consumer has read page p by now: its slot takes page p + NBUF
-          if (lane == 0 && p + NBUF < n_pages) {
-            wait_k(&s_empty[ring_slot(p)], ring_use(p));
-            const int nxt = p + NBUF;
-            const uint32_t si = ring_slot(nxt);
-            fence_proxy_async();
-            mbar_expect_tx(&s_full[si], PL::bytes);
-            bulk_g2s(s_pages + si * C::PAGE, seq_base + (size_t)(p_lo + nxt) * PL::bytes, PL::bytes, &s_full[si]);
-            issued = pg_base + nxt + 1;
-            if (nxt + kL2Ahead < n_pages)
-              prefetch_l2(seq_base + (size_t)(p_lo + nxt + kL2Ahead) * PL::bytes, PL::bytes);
+          if constexpr (PAGED) {
+            if (p + NBUF < n_pages) {   // warp-uniform
+              const int nxt = p + NBUF;
+              if (nxt >= 32 * (win + 1)) {   // slide the window; the next one loads ~20 pages ahead
+                blk_a = blk_b;
+                ++win;
+                const int i = 32 * (win + 1) + lane;
+                blk_b = i < n_pages ? __ldg(trow + i) : 0;
+              }
+              const uint8_t* src = page_at(nxt);
+              const uint8_t* far = nxt + kL2Ahead < n_pages ? page_at(nxt + kL2Ahead) : nullptr;
+              if (lane == 0) {
+                wait_k(&s_empty[ring_slot(p)], ring_use(p));
+                const uint32_t si = ring_slot(nxt);
+                fence_proxy_async();
+                mbar_expect_tx(&s_full[si], PL::bytes);
+                bulk_g2s(s_pages + si * C::PAGE, src, PL::bytes, &s_full[si]);
+                issued = pg_base + nxt + 1;
+                if (far) prefetch_l2(far, PL::bytes);
+              }
+            }
+          } else {
+            if (lane == 0 && p + NBUF < n_pages) {
+              wait_k(&s_empty[ring_slot(p)], ring_use(p));
+              const int nxt = p + NBUF;
+              const uint32_t si = ring_slot(nxt);
+              fence_proxy_async();
+              mbar_expect_tx(&s_full[si], PL::bytes);
+              bulk_g2s(s_pages + si * C::PAGE, page_at(nxt), PL::bytes, &s_full[si]);
+              issued = pg_base + nxt + 1;
+              if (nxt + kL2Ahead < n_pages)
+                prefetch_l2(page_at(nxt + kL2Ahead), PL::bytes);
+            }
           }
           __syncwarp();
         }

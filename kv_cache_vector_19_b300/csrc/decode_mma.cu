@@ -86,10 +86,11 @@ int prepare_one() {
   if constexpr (!C::SUPPORTED) {
     return TQ_OK;
   } else {
-    return cudaFuncSetAttribute(decode_mma_kernel<D, BITS, NGRP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                C::SMEM) == cudaSuccess
-               ? TQ_OK
-               : TQ_ECUDA;
+    const bool ok = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, NGRP, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) == cudaSuccess &&
+                    cudaFuncSetAttribute(decode_mma_kernel<D, BITS, NGRP, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) == cudaSuccess;
+    return ok ? TQ_OK : TQ_ECUDA;
   }
 }
 
@@ -106,7 +107,7 @@ bool plan_one(const tq_ctx* c, int batch, int kv_heads, int max_tokens, MmaPlan*
 template <int D, int BITS, int NGRP>
 int launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws,
-               cudaStream_t st) {
+               cudaStream_t st, const PageMap& pm) {
   using C = Cfg<D, BITS, NGRP>;
   if constexpr (!C::SUPPORTED) {
     return TQ_EUNSUPPORTED;
@@ -136,7 +137,10 @@ int launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, in
     a.chunk = pl.chunk;
     a.slots = pl.slots;
     a.total_pages = pl.total_pages;
-    decode_mma_kernel<D, BITS, NGRP><<<pl.grid, kThreads, C::SMEM, st>>>(a);
+    if (pm.table)
+      decode_mma_kernel<D, BITS, NGRP, true><<<pl.grid, kThreads, C::SMEM, st>>>(a, pm);
+    else
+      decode_mma_kernel<D, BITS, NGRP, false><<<pl.grid, kThreads, C::SMEM, st>>>(a, pm);
     combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
                                                           pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
@@ -176,13 +180,13 @@ bool plan_decode_mma(const tq_ctx* c, int batch, int q_heads, int kv_heads, int 
 
 int launch_decode_mma(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                       const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
-                      void* workspace, void* stream) {
+                      void* workspace, void* stream, const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int ng = dmma::ngrp_of(q_heads / kv_heads);
 #define TQ_L(DD, BB, NG)                                                                                    \
   if (c->d == DD && c->bits == BB && ng == NG)                                                              \
     return dmma::launch_one<DD, BB, NG>(c, pl, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, \
-                                        logits_out, workspace, st);
+                                        logits_out, workspace, st, pm);
   TQ_FOR_ALL(TQ_L)
 #undef TQ_L
   return TQ_EUNSUPPORTED;
@@ -209,10 +213,11 @@ int tc_prepare_one() {
   if constexpr (!C::SUPPORTED) {
     return TQ_OK;
   } else {
-    return cudaFuncSetAttribute(dtc::decode_tc_kernel<BITS, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                C::SMEM) == cudaSuccess
-               ? TQ_OK
-               : TQ_ECUDA;
+    const bool ok = cudaFuncSetAttribute(dtc::decode_tc_kernel<BITS, GP, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) == cudaSuccess &&
+                    cudaFuncSetAttribute(dtc::decode_tc_kernel<BITS, GP, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) == cudaSuccess;
+    return ok ? TQ_OK : TQ_ECUDA;
   }
 }
 
@@ -221,7 +226,7 @@ int tc_gp(int group) { return group <= 4 ? 4 : group <= 8 ? 8 : group <= 16 ? 16
 template <int BITS, int GP>
 int tc_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                   const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws,
-                  cudaStream_t st) {
+                  cudaStream_t st, const PageMap& pm) {
   using C = dtc::Cfg<BITS, GP>;
   if constexpr (!C::SUPPORTED) {
     return TQ_EUNSUPPORTED;
@@ -252,7 +257,10 @@ int tc_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
     a.chunk = pl.chunk;
     a.slots = pl.slots;
     a.total_pages = pl.total_pages;
-    dtc::decode_tc_kernel<BITS, GP><<<pl.grid, C::THREADS, C::SMEM, st>>>(a);
+    if (pm.table)
+      dtc::decode_tc_kernel<BITS, GP, true><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm);
+    else
+      dtc::decode_tc_kernel<BITS, GP, false><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm);
     dmma::combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
                                                                 pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
@@ -292,13 +300,13 @@ int prepare_decode_tc(const tq_ctx* c) {
 
 int launch_decode_tc(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                      const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
-                     void* workspace, void* stream) {
+                     void* workspace, void* stream, const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int gp = tc_gp(q_heads / kv_heads);
 #define TQ_L(BB, GG)                                                                                         \
   if (c->bits == BB && gp == GG)                                                                             \
     return tc_launch_one<BB, GG>(c, pl, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out, \
-                                 workspace, st);
+                                 workspace, st, pm);
   TQ_L(2, 4) TQ_L(2, 8) TQ_L(2, 16) TQ_L(3, 4) TQ_L(3, 8) TQ_L(3, 16)
 #undef TQ_L
   return TQ_EUNSUPPORTED;
@@ -318,10 +326,11 @@ int f4_prepare_one() {
   if constexpr (!C::SUPPORTED) {
     return TQ_OK;
   } else {
-    return cudaFuncSetAttribute(dtf::decode_f4_kernel<BITS, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                C::SMEM) == cudaSuccess
-               ? TQ_OK
-               : TQ_ECUDA;
+    const bool ok = cudaFuncSetAttribute(dtf::decode_f4_kernel<BITS, GP, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) == cudaSuccess &&
+                    cudaFuncSetAttribute(dtf::decode_f4_kernel<BITS, GP, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) == cudaSuccess;
+    return ok ? TQ_OK : TQ_ECUDA;
   }
 }
 
@@ -330,7 +339,7 @@ int f4_gp(int group) { return group <= 4 ? 4 : group <= 8 ? 8 : 0; }
 template <int BITS, int GP>
 int f4_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                   const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws,
-                  cudaStream_t st) {
+                  cudaStream_t st, const PageMap& pm) {
   using C = dtf::Cfg<BITS, GP>;
   if constexpr (!C::SUPPORTED) {
     return TQ_EUNSUPPORTED;
@@ -361,7 +370,10 @@ int f4_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
     a.chunk = pl.chunk;
     a.slots = pl.slots;
     a.total_pages = pl.total_pages;
-    dtf::decode_f4_kernel<BITS, GP><<<pl.grid, C::THREADS, C::SMEM, st>>>(a);
+    if (pm.table)
+      dtf::decode_f4_kernel<BITS, GP, true><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm);
+    else
+      dtf::decode_f4_kernel<BITS, GP, false><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm);
     dmma::combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
                                                                 pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
@@ -397,13 +409,13 @@ int prepare_decode_f4(const tq_ctx* c) {
 
 int launch_decode_f4(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                      const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
-                     void* workspace, void* stream) {
+                     void* workspace, void* stream, const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int gp = f4_gp(q_heads / kv_heads);
 #define TQ_L(BB, GG)                                                                                         \
   if (c->bits == BB && gp == GG)                                                                             \
     return f4_launch_one<BB, GG>(c, pl, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out, \
-                                 workspace, st);
+                                 workspace, st, pm);
   TQ_L(2, 4) TQ_L(2, 8) TQ_L(3, 4) TQ_L(3, 8)
 #undef TQ_L
   return TQ_EUNSUPPORTED;

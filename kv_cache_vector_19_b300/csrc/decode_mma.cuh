@@ -106,8 +106,8 @@ using namespace dev;
 
 // ---------------------------------------------------------------- the kernel
 
-template <int D, int BITS, int NGRP>
-__global__ void __launch_bounds__(kThreads, Cfg<D, BITS, NGRP>::MINB) decode_mma_kernel(Params a) {
+template <int D, int BITS, int NGRP, bool PAGED>
+__global__ void __launch_bounds__(kThreads, Cfg<D, BITS, NGRP>::MINB) decode_mma_kernel(Params a, PageMap pm) {
   using C = Cfg<D, BITS, NGRP>;
   using PL = typename C::PL;
   constexpr int NS = C::NS, PK = C::PK, PV = C::PV, KB = C::KB, GP = C::GP, BK = C::BK, BV = C::BV;
@@ -177,7 +177,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, BITS, NGRP>::MINB) decode_mma
     const int n_pages = max(0, p_hi - p_lo);
     const int slot = blockIdx.x - (seq * PM) / a.chunk;
     float* rec = a.part + ((size_t)seq * a.slots + slot) * G * (2 + D);
+    // page p of this sequence: contiguous, or through the block table (PAGED, a separate
+    // instantiation so that the contiguous kernel's address arithmetic stays as it was)
     const uint8_t* seq_base = a.cache + (size_t)seq * PM * PL::bytes;
+    auto page_g = [&](int p) -> const uint8_t* {
+      if constexpr (PAGED) return a.cache + pm.index(seq, a.kv_heads, PM, p, a.status) * PL::bytes;
+      else return seq_base + (size_t)p * PL::bytes;
+    };
 
     __syncthreads();   // the previous segment is fully done with shared memory
     // start streaming this segment's pages while the query operand is built
@@ -189,10 +195,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, BITS, NGRP>::MINB) decode_mma
         const uint32_t slot_i = (fill_base + i) % NBUF;
         fence_proxy_async();
         mbar_expect_tx(&s_mbar[slot_i], PL::bytes);
-        bulk_g2s(s_pages + slot_i * C::PAGE, seq_base + (size_t)(p_lo + i) * PL::bytes, PL::bytes, &s_mbar[slot_i]);
+        bulk_g2s(s_pages + slot_i * C::PAGE, page_g(p_lo + i), PL::bytes, &s_mbar[slot_i]);
       }
       for (int i = NBUF; i < min(n_pages, NBUF + kL2Ahead); ++i)
-        prefetch_l2(seq_base + (size_t)(p_lo + i) * PL::bytes, PL::bytes);
+        prefetch_l2(page_g(p_lo + i), PL::bytes);
     }
     fill_count = fill_base + n_pages;   // every page of the segment is issued and consumed
 
@@ -641,11 +647,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, BITS, NGRP>::MINB) decode_mma
           const uint32_t slot_i = (fill_base + nxt) % NBUF;
           fence_proxy_async();
           mbar_expect_tx(&s_mbar[slot_i], PL::bytes);
-          bulk_g2s(s_pages + slot_i * C::PAGE, seq_base + (size_t)(p_lo + nxt) * PL::bytes, PL::bytes,
+          bulk_g2s(s_pages + slot_i * C::PAGE, page_g(p_lo + nxt), PL::bytes,
                    &s_mbar[slot_i]);
         }
         const int far = nxt + kL2Ahead;
-        if (far < n_pages) prefetch_l2(seq_base + (size_t)(p_lo + far) * PL::bytes, PL::bytes);
+        if (far < n_pages) prefetch_l2(page_g(p_lo + far), PL::bytes);
       }
     }
     if (failed) break;

@@ -78,6 +78,7 @@ struct DArgs {
   const float* ck;
   const float* cv;
   int* status;
+  PageMap pm;
   int q_heads, kv_heads, group, max_tokens, pages_per_seq, splits, pages_per_split;
 };
 
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
 
   for (int p = p0; p < p1; ++p) {
     if (p * 128 >= seq_len) break;
-    const uint8_t* pg = a.cache + (seq * a.pages_per_seq + p) * (size_t)PL::bytes;
+    const uint8_t* pg = a.cache + a.pm.index((int)seq, a.kv_heads, a.pages_per_seq, p, a.status) * PL::bytes;
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(pg + PL::off_kcodes);
     const uint32_t* sg = reinterpret_cast<const uint32_t*>(pg + PL::off_signs);
     const float* nk = reinterpret_cast<const float*>(pg + PL::off_nk);
@@ -292,7 +293,8 @@ __global__ void __launch_bounds__(D) combine_kernel(const float* __restrict__ pa
 
 template <int D, int BITS>
 int launch_d(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
-             const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws, cudaStream_t st) {
+             const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws, cudaStream_t st,
+             const PageMap& pm) {
   SplitPlan sp = plan_splits(batch, kv_heads, max_tokens);
   float* qr = static_cast<float*>(ws);
   float* qs = qr + (size_t)batch * q_heads * D;
@@ -313,6 +315,7 @@ int launch_d(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_hea
   a.group = q_heads / kv_heads;
   a.max_tokens = max_tokens;
   a.pages_per_seq = sp.pages;
+  a.pm = pm;
   a.splits = sp.splits;
   a.pages_per_split = sp.pages_per_split;
   split_kernel<D, BITS><<<dim3(sp.splits, kv_heads, batch), kThreads, 0, st>>>(a);
@@ -342,12 +345,12 @@ void launch_prologue(const tq_ctx* c, const float* q, int batch, int q_heads, fl
 
 int launch_decode_simt(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_heads,
                        const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
-                       float* logits_out, void* workspace, void* stream) {
+                       float* logits_out, void* workspace, void* stream, const tq::PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define TQ_D(DD, BB)                                                                                \
   if (c->d == DD && c->bits == BB)                                                                  \
     return tq::launch_d<DD, BB>(c, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out,  \
-                                logits_out, workspace, st);
+                                logits_out, workspace, st, pm);
   TQ_D(64, 2) TQ_D(64, 3) TQ_D(64, 4) TQ_D(64, 5)
   TQ_D(128, 2) TQ_D(128, 3) TQ_D(128, 4) TQ_D(128, 5)
   TQ_D(256, 2) TQ_D(256, 3) TQ_D(256, 4) TQ_D(256, 5)

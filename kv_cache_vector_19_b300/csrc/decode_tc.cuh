@@ -187,8 +187,8 @@ __device__ __forceinline__ void expand_words(const uint32_t (&x)[4], uint32_t (&
     for (int k = 0; k < 8; ++k) r[8 * c + k] = expand_at(x[c], k);
 }
 
-template <int BITS, int GP>
-__global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Params a) {
+template <int BITS, int GP, bool PAGED>
+__global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Params a, PageMap pm) {
   using C = Cfg<BITS, GP>;
   using PL = typename C::PL;
   constexpr int D = 128, NS = C::NS, PK = C::PK, PV = C::PV, BK = C::BK, BV = C::BV, NBUF = C::NBUF;
@@ -295,7 +295,13 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
     const int p_lo = seg_lo, n_pages = max(0, min(seg_hi, valid_pages) - p_lo);
     const int slot = blockIdx.x - (seq * PM) / a.chunk;
     float* rec = a.part + ((size_t)seq * a.slots + slot) * G * (2 + D);
+    // page p of this sequence: contiguous, or through the block table (PAGED, a separate
+    // instantiation so that the contiguous kernel's address arithmetic stays as it was)
     const uint8_t* seq_base = a.cache + (size_t)seq * PM * PL::bytes;
+    auto page_g = [&](int p) -> const uint8_t* {
+      if constexpr (PAGED) return a.cache + pm.index(seq, a.kv_heads, PM, p, a.status) * PL::bytes;
+      else return seq_base + (size_t)p * PL::bytes;
+    };
     // ring slot / use of the page with segment index p (ring fills are counted over segments)
     auto ring_slot = [&](int p) { return (pg_base + p) % NBUF; };
     auto ring_use = [&](int p) { return (pg_base + p) / NBUF; };
@@ -308,11 +314,11 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
         const uint32_t si = ring_slot(i);
         fence_proxy_async();
         mbar_expect_tx(&s_full[si], PL::bytes);
-        bulk_g2s(s_pages + si * C::PAGE, seq_base + (size_t)(p_lo + i) * PL::bytes, PL::bytes, &s_full[si]);
+        bulk_g2s(s_pages + si * C::PAGE, page_g(p_lo + i), PL::bytes, &s_full[si]);
       }
       issued = pg_base + first;
       for (int i = NBUF; i < min(n_pages, NBUF + kL2Ahead); ++i)
-        prefetch_l2(seq_base + (size_t)(p_lo + i) * PL::bytes, PL::bytes);
+        prefetch_l2(page_g(p_lo + i), PL::bytes);
     }
 
     // ---- query operand of this KV head ----
@@ -474,10 +480,10 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
             const uint32_t si = ring_slot(nxt);
             fence_proxy_async();
             mbar_expect_tx(&s_full[si], PL::bytes);
-            bulk_g2s(s_pages + si * C::PAGE, seq_base + (size_t)(p_lo + nxt) * PL::bytes, PL::bytes, &s_full[si]);
+            bulk_g2s(s_pages + si * C::PAGE, page_g(p_lo + nxt), PL::bytes, &s_full[si]);
             issued = pg_base + nxt + 1;
             if (nxt + kL2Ahead < n_pages)
-              prefetch_l2(seq_base + (size_t)(p_lo + nxt + kL2Ahead) * PL::bytes, PL::bytes);
+              prefetch_l2(page_g(p_lo + nxt + kL2Ahead), PL::bytes);
           }
           __syncwarp();
         }

@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(D) dequantize_kernel(const uint8_t* __restrict
                                                        int n_tokens, const float* __restrict__ pi,
                                                        const float* __restrict__ smat, const float* __restrict__ ck,
                                                        const float* __restrict__ cv, float* __restrict__ k_out,
-                                                       float* __restrict__ v_out, int* status) {
+                                                       float* __restrict__ v_out, int* status, PageMap pm) {
   using PL = PageLayout<D, BITS>;
   constexpr int M = D, BK = BITS - 1, BV = BITS;
   constexpr int TILE = D > 128 ? 8 : 16;
@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(D) dequantize_kernel(const uint8_t* __restrict
   const int page = start / 128 + (int)blockIdx.x;
   const int lo = max(start, page * 128), hi = min(start + n_tokens, page * 128 + 128);
   if (lo >= hi) return;
-  const uint8_t* pg = cache + ((size_t)seq * pages_per_seq + page) * (size_t)PL::bytes;
+  const uint8_t* pg = cache + pm.index(seq, kv_heads, pages_per_seq, page, status) * PL::bytes;
   const uint32_t* kcodes = reinterpret_cast<const uint32_t*>(pg + PL::off_kcodes);
   const uint32_t* signs = reinterpret_cast<const uint32_t*>(pg + PL::off_signs);
   const uint32_t* vcodes = reinterpret_cast<const uint32_t*>(pg + PL::off_vcodes);
@@ -101,22 +101,23 @@ __global__ void __launch_bounds__(D) dequantize_kernel(const uint8_t* __restrict
 
 template <int D, int BITS>
 int launch_one(const tq_ctx* c, const void* cache, int batch, int kv_heads, int max_tokens, const int32_t* start_pos,
-               int n_tokens, float* k_out, float* v_out, cudaStream_t st) {
+               int n_tokens, float* k_out, float* v_out, cudaStream_t st, const PageMap& pm) {
   const dim3 grid((unsigned)((n_tokens + 127) / 128 + 1), (unsigned)(batch * kv_heads));
   dequantize_kernel<D, BITS><<<grid, D, 0, st>>>(static_cast<const uint8_t*>(cache), kv_heads, max_tokens,
                                                  (max_tokens + 127) / 128, start_pos, n_tokens, c->d_pi, c->d_s,
-                                                 c->d_ck, c->d_cv, k_out, v_out, c->d_status);
+                                                 c->d_ck, c->d_cv, k_out, v_out, c->d_status, pm);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
 }
 
 }  // namespace
 
 int launch_dequantize(const tq_ctx* c, const void* cache, int batch, int kv_heads, int max_tokens,
-                      const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream) {
+                      const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream,
+                      const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define TQ_DQ(DD, BB) \
   if (c->d == DD && c->bits == BB)   \
-    return launch_one<DD, BB>(c, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, st);
+    return launch_one<DD, BB>(c, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, st, pm);
   TQ_DQ(64, 2) TQ_DQ(64, 3) TQ_DQ(64, 4) TQ_DQ(64, 5) TQ_DQ(128, 2) TQ_DQ(128, 3) TQ_DQ(128, 4) TQ_DQ(128, 5)
   TQ_DQ(256, 2) TQ_DQ(256, 3) TQ_DQ(256, 4) TQ_DQ(256, 5)
 #undef TQ_DQ

@@ -67,6 +67,7 @@ struct QArgs {
   const float* tv;
   const float* exact;
   int* status;
+  PageMap pm;
   Geom g;
 };
 
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QArgs a) {
   for (int i = tid; i < 2 * LV; i += kThreads) reinterpret_cast<float*>(s_nv)[i] = T.nvt[i];
 
   const size_t seq = (size_t)b * a.kv_heads + h;
-  uint8_t* pg = a.cache + (seq * a.pages_per_seq + page) * (size_t)g.bytes;
+  uint8_t* pg = a.cache + a.pm.index((int)seq, a.kv_heads, a.pages_per_seq, page, a.status) * g.bytes;
   uint32_t* g_kc = reinterpret_cast<uint32_t*>(pg + g.off_kcodes);
   uint32_t* g_sg = reinterpret_cast<uint32_t*>(pg + g.off_signs);
   float* g_nk = reinterpret_cast<float*>(pg + g.off_nk);
@@ -358,7 +359,7 @@ constexpr size_t quant_smem_bytes() {
 
 template <int D>
 int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-             const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st) {
+             const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm) {
   QArgs a;
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
@@ -376,6 +377,7 @@ int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_he
   a.tv = c->d_tv;
   a.exact = c->d_exact;
   a.status = c->d_status;
+  a.pm = pm;
   a.g = geom_of(c);
   const dim3 grid((n_tokens + 127) / 128 + 1, kv_heads, batch);
   quantize_kernel<D><<<grid, kThreads, quant_smem_bytes<D>(), st>>>(a);
@@ -425,6 +427,7 @@ struct DArgs {
   const float* ck;
   const float* cv;
   int* status;
+  PageMap pm;
   int q_heads, kv_heads, group, max_tokens, pages_per_seq, splits, pages_per_split;
   Geom g;
 };
@@ -478,7 +481,7 @@ __global__ void __launch_bounds__(kDThreads) split_kernel(DArgs a) {
 
   for (int p = p0; p < p1; ++p) {
     if (p * 128 >= seq_len) break;
-    const uint8_t* pg = a.cache + (seq * a.pages_per_seq + p) * (size_t)g.bytes;
+    const uint8_t* pg = a.cache + a.pm.index((int)seq, a.kv_heads, a.pages_per_seq, p, a.status) * g.bytes;
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(pg + g.off_kcodes);
     const uint32_t* sg = reinterpret_cast<const uint32_t*>(pg + g.off_signs);
     const float* nk = reinterpret_cast<const float*>(pg + g.off_nk);
@@ -606,7 +609,8 @@ __global__ void __launch_bounds__(kDThreads) split_kernel(DArgs a) {
 
 template <int D>
 int launch_d(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
-             const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws, cudaStream_t st) {
+             const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws, cudaStream_t st,
+             const PageMap& pm) {
   const SplitPlan sp = plan_splits(batch, kv_heads, max_tokens);
   float* qr = static_cast<float*>(ws);
   float* qs = qr + (size_t)batch * q_heads * D;
@@ -627,6 +631,7 @@ int launch_d(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_hea
   a.group = q_heads / kv_heads;
   a.max_tokens = max_tokens;
   a.pages_per_seq = sp.pages;
+  a.pm = pm;
   a.splits = sp.splits;
   a.pages_per_split = sp.pages_per_split;
   a.g = geom_of(c);
@@ -645,7 +650,7 @@ __global__ void __launch_bounds__(D) dequantize_kernel(const uint8_t* __restrict
                                                        int n_tokens, const float* __restrict__ pi,
                                                        const float* __restrict__ smat, const float* __restrict__ ck,
                                                        const float* __restrict__ cv, float* __restrict__ k_out,
-                                                       float* __restrict__ v_out, int* status, Geom g) {
+                                                       float* __restrict__ v_out, int* status, Geom g, PageMap pm) {
   constexpr int KW = D / 32, TILE = D > 128 ? 8 : 16;
   __shared__ float s_uk[TILE][D];   // n_k c_K[idx], rotated frame
   __shared__ float s_uv[TILE][D];   // n_v c_V[idx], rotated frame
@@ -661,7 +666,7 @@ __global__ void __launch_bounds__(D) dequantize_kernel(const uint8_t* __restrict
   const int page = start / 128 + (int)blockIdx.x;
   const int lo = max(start, page * 128), hi = min(start + n_tokens, page * 128 + 128);
   if (lo >= hi) return;
-  const uint8_t* pg = cache + ((size_t)seq * pages_per_seq + page) * (size_t)g.bytes;
+  const uint8_t* pg = cache + pm.index(seq, kv_heads, pages_per_seq, page, status) * g.bytes;
   const uint32_t* kcodes = reinterpret_cast<const uint32_t*>(pg + g.off_kcodes);
   const uint32_t* signs = reinterpret_cast<const uint32_t*>(pg + g.off_signs);
   const uint32_t* vcodes = reinterpret_cast<const uint32_t*>(pg + g.off_vcodes);
@@ -722,11 +727,11 @@ __global__ void __launch_bounds__(D) dequantize_kernel(const uint8_t* __restrict
 
 template <int D>
 int launch_dq(const tq_ctx* c, const void* cache, int batch, int kv_heads, int max_tokens, const int32_t* start_pos,
-              int n_tokens, float* k_out, float* v_out, cudaStream_t st) {
+              int n_tokens, float* k_out, float* v_out, cudaStream_t st, const PageMap& pm) {
   const dim3 grid((unsigned)((n_tokens + 127) / 128 + 1), (unsigned)(batch * kv_heads));
   dequantize_kernel<D><<<grid, D, 0, st>>>(static_cast<const uint8_t*>(cache), kv_heads, max_tokens,
                                            (max_tokens + 127) / 128, start_pos, n_tokens, c->d_pi, c->d_s, c->d_ck,
-                                           c->d_cv, k_out, v_out, c->d_status, geom_of(c));
+                                           c->d_cv, k_out, v_out, c->d_status, geom_of(c), pm);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
 }
 
@@ -744,35 +749,36 @@ int prepare_kv2(const tq_ctx* c) {
 }
 
 int launch_quantize_kv2(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                        const int32_t* start_pos, void* cache, int max_tokens, void* stream) {
+                        const int32_t* start_pos, void* cache, int max_tokens, void* stream, const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (c->d == 64) return kv2::launch_q<64>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st);
-  if (c->d == 128) return kv2::launch_q<128>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st);
-  if (c->d == 256) return kv2::launch_q<256>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st);
+  if (c->d == 64) return kv2::launch_q<64>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
+  if (c->d == 128) return kv2::launch_q<128>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
+  if (c->d == 256) return kv2::launch_q<256>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
   return TQ_EUNSUPPORTED;
 }
 
 int launch_decode_kv2(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
                       const int32_t* seq_lens, int max_tokens, float* out, float* logits_out, void* workspace,
-                      void* stream) {
+                      void* stream, const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define TQ_D2(DD)                                                                                               \
   if (c->d == DD)                                                                                               \
     return kv2::launch_d<DD>(c, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out, workspace, \
-                             st);
+                             st, pm);
   TQ_D2(64) TQ_D2(128) TQ_D2(256)
 #undef TQ_D2
   return TQ_EUNSUPPORTED;
 }
 
 int launch_dequantize_kv2(const tq_ctx* c, const void* cache, int batch, int kv_heads, int max_tokens,
-                          const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream) {
+                          const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream,
+                          const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (c->d == 64) return kv2::launch_dq<64>(c, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, st);
+  if (c->d == 64) return kv2::launch_dq<64>(c, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, st, pm);
   if (c->d == 128)
-    return kv2::launch_dq<128>(c, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, st);
+    return kv2::launch_dq<128>(c, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, st, pm);
   if (c->d == 256)
-    return kv2::launch_dq<256>(c, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, st);
+    return kv2::launch_dq<256>(c, cache, batch, kv_heads, max_tokens, start_pos, n_tokens, k_out, v_out, st, pm);
   return TQ_EUNSUPPORTED;
 }
 

@@ -38,6 +38,7 @@ struct QArgs {
   const float* tv;
   const float* exact;   // exact-decision tables
   int* status;
+  PageMap pm;
 };
 
 // C[64][N] (row stride N+1) = A[64][D] (row stride D+1) * Bt[D][N]; 256 threads,
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
   const int lane = tid & 31;
 
   const size_t seq = (size_t)b * a.kv_heads + h;
-  uint8_t* pg = a.cache + (seq * a.pages_per_seq + page) * (size_t)PL::bytes;
+  uint8_t* pg = a.cache + a.pm.index((int)seq, a.kv_heads, a.pages_per_seq, page, a.status) * PL::bytes;
   uint32_t* g_kc = reinterpret_cast<uint32_t*>(pg + PL::off_kcodes);
   uint32_t* g_sg = reinterpret_cast<uint32_t*>(pg + PL::off_signs);
   float* g_nk = reinterpret_cast<float*>(pg + PL::off_nk);
@@ -337,7 +338,7 @@ int prepare_q() {
 
 template <int D, int BITS>
 int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-             const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st) {
+             const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm) {
   constexpr size_t smem = quant_smem_bytes<D>();
   QArgs a;
   a.k = static_cast<const __nv_bfloat16*>(k);
@@ -356,6 +357,7 @@ int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_he
   a.tv = c->d_tv;
   a.exact = c->d_exact;
   a.status = c->d_status;
+  a.pm = pm;
   dim3 grid((n_tokens + 127) / 128 + 1, kv_heads, batch);
   quantize_simt_kernel<D, BITS><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
@@ -376,11 +378,11 @@ int prepare_quantize_simt(const tq_ctx* c) {
 
 int launch_quantize_simt(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads,
                          int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
-                         void* stream) {
+                         void* stream, const tq::PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define TQ_Q(DD, BB)                                                                              \
   if (c->d == DD && c->bits == BB)                                                                \
-    return tq::launch_q<DD, BB>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st);
+    return tq::launch_q<DD, BB>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
   TQ_Q(64, 2) TQ_Q(64, 3) TQ_Q(64, 4) TQ_Q(64, 5)
   TQ_Q(128, 2) TQ_Q(128, 3) TQ_Q(128, 4) TQ_Q(128, 5)
   TQ_Q(256, 2) TQ_Q(256, 3) TQ_Q(256, 4) TQ_Q(256, 5)

@@ -72,6 +72,7 @@ struct QArgs {
   const float* cv;
   const float* tv;
   int* status;
+  PageMap pm;
 };
 
 __device__ __forceinline__ float bf16_val(uint32_t bits) { return __uint_as_float(bits << 16); }
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
     const int lo = max(start, page * 128) - page * 128;
     const int hi = min(start + a.n_tokens, page * 128 + 128) - page * 128;
     if (lo >= hi) continue;
-    uint8_t* pg = a.cache + ((size_t)seq * a.pages_per_seq + page) * (size_t)PL::bytes;
+    uint8_t* pg = a.cache + a.pm.index(seq, a.kv_heads, a.pages_per_seq, page, a.status) * PL::bytes;
     const __nv_bfloat16* kseq = a.k + (size_t)seq * a.n_tokens * D;
     const __nv_bfloat16* vseq = a.v + (size_t)seq * a.n_tokens * D;
 
@@ -533,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
 
 template <int BITS>
 int launch(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-           const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st) {
+           const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm) {
   QArgs a;
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
@@ -552,6 +553,7 @@ int launch(const tq_ctx* c, const void* k, const void* v, int batch, int kv_head
   a.cv = c->d_cv;
   a.tv = c->d_tv;
   a.status = c->d_status;
+  a.pm = pm;
   const long items = (long)batch * kv_heads * a.items_per_seq;
   const int grid = (int)(items < c->num_sms ? items : c->num_sms);
   quantize_tc_kernel<BITS><<<grid, kThreads, SMEM, st>>>(a);
@@ -574,14 +576,14 @@ int prepare_quantize_tc(const tq_ctx* c) {
 }
 
 int launch_quantize_tc(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                       const int32_t* start_pos, void* cache, int max_tokens, void* stream) {
+                       const int32_t* start_pos, void* cache, int max_tokens, void* stream, const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->d != 128 || !c->d_qblob) return TQ_EUNSUPPORTED;
   switch (c->bits) {
-    case 2: return qtc::launch<2>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st);
-    case 3: return qtc::launch<3>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st);
-    case 4: return qtc::launch<4>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st);
-    case 5: return qtc::launch<5>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st);
+    case 2: return qtc::launch<2>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
+    case 3: return qtc::launch<3>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
+    case 4: return qtc::launch<4>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
+    case 5: return qtc::launch<5>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
     default: return TQ_EUNSUPPORTED;
   }
 }

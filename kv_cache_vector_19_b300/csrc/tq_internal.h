@@ -25,6 +25,30 @@ inline size_t page_bytes(int d, int bits, int m) {
   return (size_t)kPage * ((size_t)(bits - 1) * d / 8 + m / 8 + 8 + (size_t)bits * d / 8 + 4);
 }
 
+// Where the pages of a call live.  table == nullptr: the contiguous cache
+// [batch][kv_heads][pages_per_seq][page].  Otherwise a pool of blocks, each the kv_heads pages of
+// 128 consecutive token slots (page (blk, h) at page index blk * kv_heads + h), and
+// table[b * stride + p] the block that holds logical page p of batch row b; a block id outside
+// [0, n_blocks) is clamped into it and sets kFlagBounds, so no access leaves the pool.
+struct PageMap {
+  const int32_t* table = nullptr;
+  int stride = 0;
+  int n_blocks = 0;
+#ifdef __CUDACC__
+  // Page index of logical page p of sequence seq = b * kv_heads + h.
+  __device__ __forceinline__ size_t index(int seq, int kv_heads, int pages_per_seq, int p, int* status) const {
+    if (table == nullptr) return (size_t)seq * pages_per_seq + p;
+    const int b = seq / kv_heads, h = seq - b * kv_heads;
+    int blk = __ldg(table + (size_t)b * stride + p);
+    if ((unsigned)blk >= (unsigned)n_blocks) {
+      atomicOr(status, kFlagBounds);
+      blk = blk < 0 ? 0 : n_blocks - 1;
+    }
+    return (size_t)blk * kv_heads + h;
+  }
+#endif
+};
+
 // Decode split plan shared by the workspace query and the launch.
 struct SplitPlan {
   int pages, splits, pages_per_split;
@@ -78,19 +102,23 @@ namespace tq {
 int prepare_quantize_tc(const tq_ctx* c);
 int launch_selftest_wait(const tq_ctx* c, void* stream);
 int launch_dequantize(const tq_ctx* c, const void* cache, int batch, int kv_heads, int max_tokens,
-                      const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream);
+                      const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream,
+    const PageMap& pm = PageMap());
 // Few tokens per sequence (appends): one CTA per new vector pair.
 constexpr int kFewTokens = 8;
 int launch_quantize_few(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                        const int32_t* start_pos, void* cache, int max_tokens, void* stream);
+                        const int32_t* start_pos, void* cache, int max_tokens, void* stream,
+    const PageMap& pm = PageMap());
 int launch_quantize_tc(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                       const int32_t* start_pos, void* cache, int max_tokens, void* stream);
+                       const int32_t* start_pos, void* cache, int max_tokens, void* stream,
+    const PageMap& pm = PageMap());
 }  // namespace tq
 
 // Kernel launchers (return TQ_OK or TQ_ECUDA).
 int launch_quantize_simt(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
                          int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
-                         void* stream);
+                         void* stream,
+    const tq::PageMap& pm = tq::PageMap());
 namespace tq {
 int prepare_decode_mma(const tq_ctx* c);
 bool plan_pages(long ctas, int batch, int kv_heads, int max_tokens, MmaPlan* p);
@@ -98,7 +126,8 @@ bool plan_decode_mma(const tq_ctx* c, int batch, int q_heads, int kv_heads, int 
 bool plan_decode_tc(const tq_ctx* c, int batch, int q_heads, int kv_heads, int max_tokens, MmaPlan* p);
 int launch_decode_mma(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                       const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
-                      void* workspace, void* stream);
+                      void* workspace, void* stream,
+    const PageMap& pm = PageMap());
 size_t decode_mma_workspace(const tq_ctx* c, const MmaPlan& pl, int batch, int q_heads, int kv_heads);
 // tcgen05 decode (head_dim 128, b in {2, 3}, up to 16 query heads per KV head); same plan,
 // workspace and partial records as the mma.sync kernel.
@@ -108,7 +137,8 @@ bool decode_tc_preferred(const tq_ctx* c, int q_heads, int kv_heads);
 int prepare_decode_tc(const tq_ctx* c);
 int launch_decode_tc(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                      const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
-                     void* workspace, void* stream);
+                     void* workspace, void* stream,
+    const PageMap& pm = PageMap());
 // tcgen05 decode with 4-bit (e2m1) operands: head_dim 128, b in {2, 3}, up to 8 query heads
 // per KV head; same plan, workspace and partial records as the mma.sync kernel.
 bool decode_f4_supported(const tq_ctx* c, int q_heads, int kv_heads);
@@ -116,7 +146,8 @@ bool plan_decode_f4(const tq_ctx* c, int batch, int q_heads, int kv_heads, int m
 int prepare_decode_f4(const tq_ctx* c);
 int launch_decode_f4(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                      const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
-                     void* workspace, void* stream);
+                     void* workspace, void* stream,
+    const PageMap& pm = PageMap());
 // tq_attn_decode's argument checks except the workspace (TQ_OK or its error code).
 int check_decode_args(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
                       const int32_t* seq_lens, int max_tokens, const float* out, const float* logits_out);
@@ -136,14 +167,18 @@ int launch_topk(const tq_ctx* c, const float* logits, const int32_t* seq_lens, i
 // counts and m read from the context.
 int prepare_kv2(const tq_ctx* c);
 int launch_quantize_kv2(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                        const int32_t* start_pos, void* cache, int max_tokens, void* stream);
+                        const int32_t* start_pos, void* cache, int max_tokens, void* stream,
+    const PageMap& pm = PageMap());
 int launch_decode_kv2(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
                       const int32_t* seq_lens, int max_tokens, float* out, float* logits_out, void* workspace,
-                      void* stream);
+                      void* stream,
+    const PageMap& pm = PageMap());
 int launch_dequantize_kv2(const tq_ctx* c, const void* cache, int batch, int kv_heads, int max_tokens,
-                          const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream);
+                          const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream,
+    const PageMap& pm = PageMap());
 }  // namespace tq
 
 int launch_decode_simt(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
                        const void* cache, const int32_t* seq_lens, int max_tokens, float* out,
-                       float* logits_out, void* workspace, void* stream);
+                       float* logits_out, void* workspace, void* stream,
+    const tq::PageMap& pm = tq::PageMap());

@@ -24,6 +24,12 @@ values: b bits):
   Value codes: within one coordinate's four words, token slot tau sits at
       kb = tau>>5, h = (tau>>4)&1, c = (tau>>2)&3, e = tau&3, word = c, bit = 2*kb+h+8*e
 
+Paged pool (``paged_page_offset``, ``gather_paged``): the same pages kept in a pool of blocks
+that sequences borrow in any order, as a PagedAttention-style serving engine holds its cache
+([BLOG] 3.5, vLLM; [3BITS] "vLLM").  A block is the kv_heads pages of 128 consecutive token
+slots, page (block, h) at byte (block * kv_heads + h) * page_bytes of the pool, and a table
+row per sequence names the block of each of its logical pages.
+
 Format version 2 (the ``*_kv`` functions) generalises version 1 to separate key and value
 widths and to keys without the QJL stage ([3BITS] "Python + HuggingFace": a cache object
 built with key_bits and value_bits, and a stage-1-only quantizer returning indices and
@@ -185,3 +191,22 @@ def unpack_tokens(d, b, m, cache_bytes, n_pages, batch, kv_head, n_tokens, kv_he
     """Per-token arrays for slots [0, n_tokens) of one (batch, kv_head) from a whole
     version-1 cache buffer laid out [batch][kv_head][n_pages][page]."""
     return unpack_tokens_kv(d, b - 1, b, m, cache_bytes, n_pages, batch, kv_head, n_tokens, kv_heads)
+
+
+def paged_page_offset(block, kv_head, kv_heads, page_bytes):
+    """Byte offset of the page of ``kv_head`` in ``block`` of a paged pool."""
+    return (block * kv_heads + kv_head) * page_bytes
+
+
+def gather_paged(pool_bytes, block_table, batch, kv_heads, page_bytes, n_pages):
+    """The contiguous cache [batch][kv_head][n_pages][page] that a paged pool and its block
+    table (int [batch][>= n_pages]) stand for: logical page p of (b, h) is the page of h in
+    block block_table[b][p]."""
+    out = np.zeros(batch * kv_heads * n_pages * page_bytes, dtype=np.uint8)
+    for b in range(batch):
+        for h in range(kv_heads):
+            for p in range(n_pages):
+                src = paged_page_offset(int(block_table[b][p]), h, kv_heads, page_bytes)
+                dst = ((b * kv_heads + h) * n_pages + p) * page_bytes
+                out[dst:dst + page_bytes] = pool_bytes[src:src + page_bytes]
+    return out
