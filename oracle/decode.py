@@ -15,6 +15,12 @@ reads kv head floor(h / G) with G = Hq / Hkv (consecutive grouping); an empty se
 Keys without the QJL stage (tok_k["sigma"] is None; [3BITS] "Python + HuggingFace" and its
 remark that the llama.cpp forks switch QJL off) score by the Lloyd-Max term alone.
 
+Sparse V ([3BITS] llama.cpp section, the format list: positions with low attention weights
+are skipped during decoding) is ``attend_sparse_v``.  The pages fix neither the threshold nor
+the normalisation; the reading taken: with p_t = exp(l_t - max l), a position whose p_t is
+below theta leaves the weighted sum of values, while the softmax denominator keeps every
+position (the scores are computed either way; what is skipped is the value work).
+
 Two routes are given.  Route A reconstructs every key and value in the original frame
 (plain definition).  Route B works in the rotated frame (q~ = Pi q, q_s = S q, output
 rotated back once by Pi^T); it is mathematically identical and serves as an internal
@@ -43,6 +49,26 @@ def attend_route_a(q, tok_k, tok_v, Pi, S, cb_k, cb_v):
     p = _softmax(logits)
     vhat = quant.reconstruct_values(tok_v["idx"], tok_v["n"], Pi, cb_v[0])
     return p @ vhat, logits
+
+
+def attend_sparse_v(q, tok_k, tok_v, Pi, S, cb_k, cb_v, theta):
+    """Sparse V: route A with the values of positions whose p_t = exp(l_t - max l) < theta
+    dropped from the numerator only.  Returns (out [d], logits [T], skipped) where
+    skipped = sum over dropped t of p_t ||v^_t|| / sum_t p_t bounds the change against the
+    dense output, and against any evaluation that drops a subset of these positions."""
+    d = Pi.shape[0]
+    T = len(tok_k["n"])
+    if T == 0:
+        return np.zeros(d), np.zeros(0), 0.0
+    khat = quant.reconstruct_keys_any(tok_k, Pi, S, cb_k[0])
+    logits = khat @ np.asarray(q, dtype=np.float64) / np.sqrt(d)
+    e = np.exp(logits - np.max(logits))
+    keep = e >= theta
+    vhat = quant.reconstruct_values(tok_v["idx"], tok_v["n"], Pi, cb_v[0])
+    den = np.sum(e)
+    out = (np.where(keep, e, 0.0) @ vhat) / den
+    skipped = float(np.sum(np.where(keep, 0.0, e) * np.linalg.norm(vhat, axis=1)) / den)
+    return out, logits, skipped
 
 
 def attend_route_b(q, tok_k, tok_v, Pi, S, cb_k, cb_v):
