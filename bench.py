@@ -515,7 +515,9 @@ def run_case(args, w):
     wl = workloads.preset(w.name, tokens=args.tokens or w.tokens, decode_steps=1)
     data = workloads.generate(wl)
     B, H, Hq, T, d = wl.batch, wl.kv_heads, wl.q_heads, wl.tokens, wl.d
-    ctx = tq.Context(d, wl.b, seed=wl.seed)
+    ctx = tq.Context(d, wl.b, seed=wl.seed, decode_path=args.decode_path)
+    if args.sparse_v:
+        ctx.set_sparse_v(args.sparse_v)
     k, v = data["k"].cuda(), data["v"].cuda()
     zero = torch.zeros(B, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -538,7 +540,7 @@ def run_case(args, w):
         call = quantize
     else:
         quantize()
-        q = data["q"][0].cuda().contiguous()
+        q = (data["q"][0] * args.q_scale).cuda().contiguous()
         lens = torch.full((B,), wl.tokens, dtype=torch.int32, device="cuda")
         if args.kernel_case == "decode":
             ws = ctx.alloc_workspace(B, Hq, H, T)
@@ -574,7 +576,10 @@ def run_case(args, w):
     ctx.close()
     if st != tq.TQ_OK:
         raise SystemExit(f"device status: {tq.tq_status_string(st)}")
-    print(f"{args.kernel_case} case{' (paged pool)' if args.paged else ''}: {w.name}, {wl.tokens} tokens, "
+    extra = (" (paged pool)" if args.paged else "") + (f" (sparse V {args.sparse_v:g})" if args.sparse_v else "")
+    extra += (f" (queries x{args.q_scale:g})" if args.q_scale != 1.0 else "")
+    extra += (f" ({args.decode_path} decode)" if args.decode_path != "auto" else "")
+    print(f"{args.kernel_case} case{extra}: {w.name}, {wl.tokens} tokens, "
           f"{args.warmup + args.steps} calls, status ok, "
           f"{ms * 1e3:.1f} us per call (back to back, cache {cache_mb:.0f} MB)", flush=True)
     return 0
@@ -593,6 +598,11 @@ def main():
                     help="run one kernel of the workload alone (profiling case), no JSON line")
     ap.add_argument("--tokens", type=int, default=0, help="prefill length of --kernel-case (default: workload's)")
     ap.add_argument("--topk", type=int, default=100, help="k of --kernel-case scan")
+    ap.add_argument("--sparse-v", type=float, default=0.0, help="Sparse V threshold of the kernel cases")
+    ap.add_argument("--q-scale", type=float, default=1.0,
+                    help="query scale of the kernel cases (larger: more peaked attention)")
+    ap.add_argument("--decode-path", default="auto", choices=["auto", "simt", "mma", "tc", "tc4"],
+                    help="decode kernel of the kernel cases")
     ap.add_argument("--paged", action="store_true",
                     help="--kernel-case quantize / decode on a block pool through a shuffled block table")
     args = ap.parse_args()

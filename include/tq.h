@@ -247,6 +247,19 @@ int tq_ip_topk(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv
 int tq_dequantize_kv(const tq_ctx* ctx, const void* cache, int batch, int kv_heads, int max_tokens,
                      const int32_t* start_pos, int n_tokens, float* k_out, float* v_out, void* stream);
 
+/* Sparse V ([3BITS] llama.cpp section, the format list: positions with low attention weights
+ * are skipped during decoding): with p_t = exp(l_t - m), a position whose p_t < threshold
+ * contributes no value to the attention output; the softmax denominator still counts every
+ * position (the scores are computed either way; the value work is what is skipped).  m is
+ * the running maximum of the kernel's pass over the cache (each split its own), which never
+ * exceeds the true maximum: a decode keeps every position that the same rule with the true
+ * maximum keeps, and possibly more, so its output differs from the rule's definition by at
+ * most sum over the definition's skipped t of p_t ||v^_t|| / sum_t p_t.  threshold 0 (the
+ * default) is dense attention; 0 <= threshold <= 1, else TQ_EINVAL.  Logits are unaffected.
+ * Applies to every later decode call of the context (tq_attn_decode and its _paged and
+ * _noalloc forms); tq_ip_topk's estimates do not depend on it. */
+int tq_ctx_set_sparse_v(tq_ctx* ctx, float threshold);
+
 /* Paged (block-table) cache: the compressed pages live in a pool of blocks that sequences
  * borrow in any order, the layout of a PagedAttention-style serving engine ([BLOG] 3.5 "Другие
  * инструменты и фреймворки", vLLM: PagedAttention; [3BITS] "vLLM": the TurboQuant attention

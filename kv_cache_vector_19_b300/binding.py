@@ -59,6 +59,7 @@ _SIGS = {
     "tq_ip_topk_workspace_bytes": (_c_size, [_vp, _c_int, _c_int, _c_int, _c_int]),
     "tq_ip_topk": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_size,
                             _vp]),
+    "tq_ctx_set_sparse_v": (_c_int, [_vp, ctypes.c_float]),
     "tq_paged_pool_bytes": (_c_size, [_vp, _c_int, _c_int]),
     "tq_quantize_kv_paged": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _vp, _c_int, _vp]),
     "tq_attn_decode_paged": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _c_int, _vp, _vp, _vp,
@@ -240,6 +241,12 @@ class Context:
         code = DECODE_PATHS[path] if isinstance(path, str) else int(path)
         _check("tq_ctx_set_decode_path", lib().tq_ctx_set_decode_path(self._ctx, code))
         self.decode_path = path
+
+    def set_sparse_v(self, threshold):
+        """Sparse V: positions with p_t = exp(l_t - running max) below threshold add no value
+        (0 = dense attention, the default)."""
+        _check("tq_ctx_set_sparse_v", lib().tq_ctx_set_sparse_v(self._ctx, float(threshold)))
+        self.sparse_v = float(threshold)
 
     def close(self):
         if self._ctx:

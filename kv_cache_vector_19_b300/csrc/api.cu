@@ -356,6 +356,12 @@ extern "C" int tq_ctx_set_decode_path(tq_ctx* ctx, int path) {
   return TQ_OK;
 }
 
+extern "C" int tq_ctx_set_sparse_v(tq_ctx* ctx, float threshold) {
+  if (!ctx || !(threshold >= 0.f && threshold <= 1.f)) return TQ_EINVAL;   // NaN fails too
+  ctx->sparse_v = threshold;
+  return TQ_OK;
+}
+
 namespace {
 
 // Kernel a decode call takes: TQ_DECODE_SIMT / _MMA / _TC, or TQ_EUNSUPPORTED.  The bit-plane

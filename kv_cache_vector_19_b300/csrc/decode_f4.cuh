@@ -203,7 +203,7 @@ __device__ __forceinline__ float piece_scale(float m) {
 }
 
 template <int BITS, int GP, bool PAGED>
-__global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Params a, PageMap pm) {
+__global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Params a, PageMap pm, float sparse_v) {
   using C = Cfg<BITS, GP>;
   using PL = typename C::PL;
   constexpr int D = 128, NS = C::NS, PK = C::PK, PV = C::PV, BK = C::BK, BV = C::BV, NBUF = C::NBUF;
@@ -753,8 +753,9 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
           uint32_t wb[HPT];
 #pragma unroll
           for (int h = 0; h < HPT; ++h) {
-            const float pw = lg[h] == -INFINITY ? 0.f : __expf(lg[h] - m_run[h]);
-            l_part[h] += pw;
+            float pw = lg[h] == -INFINITY ? 0.f : __expf(lg[h] - m_run[h]);
+            l_part[h] += pw;                   // the denominator keeps every position
+            if (pw < sparse_v) pw = 0.f;       // Sparse V: the position's value is skipped
             uint32_t t = min(__float2uint_rn(pw * nvr * kWScale), 65535u);
             t = (t | (t << 8)) & 0x00FF00FFu;
             t = (t | (t << 4)) & 0x0F0F0F0Fu;

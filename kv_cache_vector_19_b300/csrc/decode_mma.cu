@@ -138,9 +138,9 @@ int launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, in
     a.slots = pl.slots;
     a.total_pages = pl.total_pages;
     if (pm.table)
-      decode_mma_kernel<D, BITS, NGRP, true><<<pl.grid, kThreads, C::SMEM, st>>>(a, pm);
+      decode_mma_kernel<D, BITS, NGRP, true><<<pl.grid, kThreads, C::SMEM, st>>>(a, pm, c->sparse_v);
     else
-      decode_mma_kernel<D, BITS, NGRP, false><<<pl.grid, kThreads, C::SMEM, st>>>(a, pm);
+      decode_mma_kernel<D, BITS, NGRP, false><<<pl.grid, kThreads, C::SMEM, st>>>(a, pm, c->sparse_v);
     combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
                                                           pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
@@ -258,9 +258,9 @@ int tc_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
     a.slots = pl.slots;
     a.total_pages = pl.total_pages;
     if (pm.table)
-      dtc::decode_tc_kernel<BITS, GP, true><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm);
+      dtc::decode_tc_kernel<BITS, GP, true><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm, c->sparse_v);
     else
-      dtc::decode_tc_kernel<BITS, GP, false><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm);
+      dtc::decode_tc_kernel<BITS, GP, false><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm, c->sparse_v);
     dmma::combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
                                                                 pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
@@ -371,9 +371,9 @@ int f4_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
     a.slots = pl.slots;
     a.total_pages = pl.total_pages;
     if (pm.table)
-      dtf::decode_f4_kernel<BITS, GP, true><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm);
+      dtf::decode_f4_kernel<BITS, GP, true><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm, c->sparse_v);
     else
-      dtf::decode_f4_kernel<BITS, GP, false><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm);
+      dtf::decode_f4_kernel<BITS, GP, false><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm, c->sparse_v);
     dmma::combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
                                                                 pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
     return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;

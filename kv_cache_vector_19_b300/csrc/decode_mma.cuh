@@ -107,7 +107,7 @@ using namespace dev;
 // ---------------------------------------------------------------- the kernel
 
 template <int D, int BITS, int NGRP, bool PAGED>
-__global__ void __launch_bounds__(kThreads, Cfg<D, BITS, NGRP>::MINB) decode_mma_kernel(Params a, PageMap pm) {
+__global__ void __launch_bounds__(kThreads, Cfg<D, BITS, NGRP>::MINB) decode_mma_kernel(Params a, PageMap pm, float sparse_v) {
   using C = Cfg<D, BITS, NGRP>;
   using PL = typename C::PL;
   constexpr int NS = C::NS, PK = C::PK, PV = C::PV, KB = C::KB, GP = C::GP, BK = C::BK, BV = C::BV;
@@ -608,9 +608,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, BITS, NGRP>::MINB) decode_mma
         for (int u = 0; u < NGRP; ++u) {
           const float p0 = lg_prev[u][0] == -INFINITY ? 0.f : __expf(lg_prev[u][0] - m_run[u]);
           const float p1 = lg_prev[u][1] == -INFINITY ? 0.f : __expf(lg_prev[u][1] - m_run[u]);
-          l_part[u] += p0 + p1;
-          const float x0 = p0 * nv_prev[0] * inv_n * v_igamma * kSB;
-          const float x1 = p1 * nv_prev[1] * inv_n * v_igamma * kSB;
+          l_part[u] += p0 + p1;   // the denominator keeps every position
+          // Sparse V: a position below the threshold contributes no value
+          const float x0 = (p0 < sparse_v ? 0.f : p0) * nv_prev[0] * inv_n * v_igamma * kSB;
+          const float x1 = (p1 < sparse_v ? 0.f : p1) * nv_prev[1] * inv_n * v_igamma * kSB;
           const uint32_t hi = cvt_e4m3x2(x1, x0);
           const float2 hf = e4m3x2_to_f2(hi);
           const uint32_t lo = cvt_e4m3x2(16.f * (x1 - hf.y), 16.f * (x0 - hf.x));   // second piece x16

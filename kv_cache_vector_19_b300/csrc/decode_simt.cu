@@ -79,6 +79,7 @@ struct DArgs {
   const float* cv;
   int* status;
   PageMap pm;
+  float sparse_v;       // Sparse V threshold (0: dense)
   int q_heads, kv_heads, group, max_tokens, pages_per_seq, splits, pages_per_split;
 };
 
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
   __shared__ float s_qs[kMaxG][D];
   __shared__ float s_p[kMaxG][128];
   __shared__ float s_nv[128];
+  __shared__ int s_keep[128];   // some head keeps the position's value (Sparse V)
   __shared__ float s_m[kMaxG], s_l[kMaxG], s_alpha[kMaxG];
   __shared__ float s_ck[32], s_cv[32];
 
@@ -148,6 +150,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
       gmm = gm[t];
     }
     s_nv[t] = valid ? nv[t] : 0.f;
+    s_keep[t] = 0;
     for (int hc = 0; hc < G; hc += 4) {
       float am[4] = {0.f, 0.f, 0.f, 0.f}, aq[4] = {0.f, 0.f, 0.f, 0.f};
       if (valid) {
@@ -199,8 +202,10 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
         float sum = 0.f;
         for (int i = lane; i < 128; i += 32) {
           float e = (m_new == -INFINITY) ? 0.f : expf(s_p[hh][i] - m_new);
+          sum += e;   // the denominator keeps every position
+          if (e < a.sparse_v) e = 0.f;   // Sparse V: the value of this position is skipped
+          else if (e > 0.f) s_keep[i] = 1;
           s_p[hh][i] = e;
-          sum += e;
         }
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
@@ -227,6 +232,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
         for (int hh = 0; hh < kMaxG; ++hh)
           if (hh < G) o[hh][u] *= s_alpha[hh];
         for (int s = 0; s < nvalid; ++s) {
+          if (!s_keep[s]) continue;   // no head keeps this position (uniform over the block)
           int w, bit;
           slot_pos(s, w, bit);
           int idx = 0;
@@ -316,6 +322,7 @@ int launch_d(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_hea
   a.max_tokens = max_tokens;
   a.pages_per_seq = sp.pages;
   a.pm = pm;
+  a.sparse_v = c->sparse_v;
   a.splits = sp.splits;
   a.pages_per_split = sp.pages_per_split;
   split_kernel<D, BITS><<<dim3(sp.splits, kv_heads, batch), kThreads, 0, st>>>(a);

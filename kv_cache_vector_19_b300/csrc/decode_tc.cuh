@@ -188,7 +188,7 @@ __device__ __forceinline__ void expand_words(const uint32_t (&x)[4], uint32_t (&
 }
 
 template <int BITS, int GP, bool PAGED>
-__global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Params a, PageMap pm) {
+__global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Params a, PageMap pm, float sparse_v) {
   using C = Cfg<BITS, GP>;
   using PL = typename C::PL;
   constexpr int D = 128, NS = C::NS, PK = C::PK, PV = C::PV, BK = C::BK, BV = C::BV, NBUF = C::NBUF;
@@ -711,9 +711,10 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_tc_kernel(Pa
           for (int h = 0; h < HPT; h += 2) {
             const float p0 = lg[h] == -INFINITY ? 0.f : __expf(lg[h] - m_run[h]);
             const float p1 = lg[h + 1] == -INFINITY ? 0.f : __expf(lg[h + 1] - m_run[h + 1]);
-            l_part[h] += p0;
+            l_part[h] += p0;   // the denominator keeps every position
             l_part[h + 1] += p1;
-            const float x0 = p0 * xs, x1 = p1 * xs;
+            // Sparse V: a position below the threshold contributes no value
+            const float x0 = (p0 < sparse_v ? 0.f : p0) * xs, x1 = (p1 < sparse_v ? 0.f : p1) * xs;
             const uint32_t hi2 = cvt_e4m3x2(x1, x0);
             const float2 hf = e4m3x2_to_f2(hi2);
             const uint32_t lo2 = cvt_e4m3x2(16.f * (x1 - hf.y), 16.f * (x0 - hf.x));

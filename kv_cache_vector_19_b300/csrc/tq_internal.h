@@ -90,6 +90,7 @@ struct tq_ctx {
   float asum_k = 0.f, asum_v = 0.f;
   int num_sms = 148;
   int decode_path = 0;   // TQ_DECODE_*
+  float sparse_v = 0.f;  // Sparse V threshold on p_t = exp(l_t - running max); 0: dense
   // head_dim 128: fp16 B operands of the tensor-core quantizer, no-swizzle K-major layout:
   // 256 Pi as hi, lo and 256 S' as hi, lo (each 128 x 128, 32 KB)
   uint8_t* d_qblob = nullptr;
