@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
   constexpr int HPT = C::HPT, kThreads = C::THREADS, ASB = C::ASB, AVB = C::AVB, TS = C::TS;
   constexpr int kWarpWV = C::WV, kWarpsAll = C::WARPS;
   extern __shared__ __align__(1024) unsigned char smem[];
+  pdl_trigger();   // the combine grid may launch once every CTA of this grid is running
   uint8_t* s_pages = smem + C::OFF_PAGES;
   uint8_t* s_bs = smem + C::OFF_BS;
   uint8_t* s_bv = smem + C::OFF_BV;
@@ -383,6 +384,7 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
     }
 
     // ---- query operand of this KV head ----
+    pdl_wait();   // q~ and q_s of the prologue grid (at once after the first segment)
     for (int e = tid; e < GP * 2 * D; e += kThreads) {
       const int hh = e / (2 * D), rem = e % (2 * D), which = rem / D, j = rem % D;
       float v = 0.f;

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(4 * D) combine_kernel(const float* __restrict_
   __shared__ float s_r[4][D];
   __shared__ float s_w[512];
   __shared__ float s_norm;
+  pdl_wait();   // the decode grid's partial records (at once when launched without the attribute)
   const int hq = blockIdx.x, b = blockIdx.y;
   const size_t row = (size_t)b * q_heads + hq;
   const int seq = b * kv_heads + hq / group, hh = hq % group;
@@ -370,13 +371,29 @@ int f4_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
     a.chunk = pl.chunk;
     a.slots = pl.slots;
     a.total_pages = pl.total_pages;
-    if (pm.table)
-      dtf::decode_f4_kernel<BITS, GP, true><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm, c->sparse_v);
-    else
-      dtf::decode_f4_kernel<BITS, GP, false><<<pl.grid, C::THREADS, C::SMEM, st>>>(a, pm, c->sparse_v);
-    dmma::combine_kernel<D><<<dim3(q_heads, batch), 4 * D, 0, st>>>(part, c->d_pi, out, q_heads, kv_heads, a.group,
-                                                                pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
-    return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
+    // The decode and the combine are launched with programmatic stream serialization: the
+    // decode grid starts its set-up and first page loads while the prologue runs (it reads
+    // nothing the prologue writes before its pdl_wait, and the prologue itself starts only
+    // after all earlier work), and the combine grid launches as the decode's CTAs finish.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.grid);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = pm.table ? cudaLaunchKernelEx(&cfg, dtf::decode_f4_kernel<BITS, GP, true>, a, pm, c->sparse_v)
+                             : cudaLaunchKernelEx(&cfg, dtf::decode_f4_kernel<BITS, GP, false>, a, pm, c->sparse_v);
+    if (e != cudaSuccess) return TQ_ECUDA;
+    cfg.gridDim = dim3(q_heads, batch);
+    cfg.blockDim = dim3(4 * D);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, dmma::combine_kernel<D>, (const float*)part, (const float*)c->d_pi, out, q_heads,
+                           kv_heads, a.group, pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
   }
 }
 

@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(4 * D) prologue_kernel(const float* __restrict
   // 4 D threads: part p = tid / D sums k over its quarter of [0, D) with all of its matrix
   // loads in flight at once (the matrices are usually out of L2 when a decode starts)
   constexpr int KQ = D / 4;
+  pdl_trigger();   // the decode grid may start its set-up; it waits for q~, q_s at pdl_wait
   __shared__ float sq[D];
   __shared__ float s_a[4][D], s_s[4][D];
   const size_t row = (size_t)blockIdx.y * q_heads + blockIdx.x;

@@ -49,6 +49,15 @@ struct PageMap {
 #endif
 };
 
+#ifdef __CUDACC__
+// Programmatic dependent launch.  pdl_trigger: the next grid of the stream, when launched with
+// programmatic stream serialization, may start now (it still waits at its own pdl_wait).
+// pdl_wait: blocks until the preceding grid has completed and its memory operations are
+// visible; returns at once in a grid launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
+
 // Decode split plan shared by the workspace query and the launch.
 struct SplitPlan {
   int pages, splits, pages_per_split;
