@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "dev_common.cuh"
 #include "exact.cuh"
 #include "layout.cuh"
 #include "tq_internal.h"
@@ -60,6 +61,28 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
     if (threadIdx.x == 0 && t == 0) atomicOr(status, kFlagBounds);
     return;
   }
+  // Every fetch that does not wait for a result starts now, so that the chain below meets
+  // one memory latency instead of one per step: S'^T and the near tables into L2 (the
+  // projection and the near tests come later), the books into shared memory, and this
+  // thread's columns of Pi^T and S'^T into registers (head_dim <= 128; at 256 the thread budget
+  // is 64 registers and the columns are loaded in the products' loops).
+  __shared__ float s_tk[LK], s_tv[LV], s_ck[LK];
+  if (threadIdx.x == 0) {
+    dev::prefetch_l2(spt, (uint32_t)(D * M * sizeof(float)));
+    dev::prefetch_l2(exact_tabs + exact::tables_floats(D) - (6 * 32 + 2 * 64), (6 * 32 + 2 * 64) * sizeof(float));
+  }
+  if (threadIdx.x < LK - 1) s_tk[threadIdx.x] = tk[threadIdx.x];
+  if (threadIdx.x < LV - 1) s_tv[threadIdx.x] = tv[threadIdx.x];
+  if (threadIdx.x < LK) s_ck[threadIdx.x] = ck[threadIdx.x];
+  constexpr bool kColumnInRegs = D <= 128;
+  float pcol[kColumnInRegs ? KQ : 1], scol[kColumnInRegs ? KQ : 1];
+  if constexpr (kColumnInRegs) {
+#pragma unroll
+    for (int cc = 0; cc < KQ; ++cc) {
+      pcol[cc] = __ldg(pit + (size_t)(qp * KQ + cc) * D + j);
+      scol[cc] = __ldg(spt + (size_t)(qp * KQ + cc) * M + j);
+    }
+  }
   const int pos = start + t, page = pos >> 7, slot = pos & 127;
   uint8_t* pg = cache + pm.index(seq, kv_heads, pages_per_seq, page, status) * PL::bytes;
   const size_t row = ((size_t)seq * n_tokens + t) * D;
@@ -79,7 +102,9 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
 #pragma unroll
     for (int cc = 0; cc < KQ; ++cc) {
       const int c = qp * KQ + cc;
-      const float p = pit[(size_t)c * D + j];
+      float p;
+      if constexpr (kColumnInRegs) p = pcol[cc];
+      else p = pit[(size_t)c * D + j];
       pa = fmaf(p, s_xk[c], pa);
       pb = fmaf(p, s_xv[c], pb);
     }
@@ -94,9 +119,9 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
   const float uk = yk * ik, uv = yv * iv;
   int idx = 0, vidx = 0;
 #pragma unroll
-  for (int q = 0; q < LK - 1; ++q) idx += uk >= tk[q] ? 1 : 0;
+  for (int q = 0; q < LK - 1; ++q) idx += uk >= s_tk[q] ? 1 : 0;
 #pragma unroll
-  for (int q = 0; q < LV - 1; ++q) vidx += uv >= tv[q] ? 1 : 0;
+  for (int q = 0; q < LV - 1; ++q) vidx += uv >= s_tv[q] ? 1 : 0;
   // codes next to a boundary are taken again exactly (exact.cuh), each warp for its own 32
   // coordinates (the warps of the four quarters repeat the same decisions)
   const exact::Tables T = exact::tables(exact_tabs, D);
@@ -129,7 +154,7 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
       }
     }
   }
-  const float r = yk - nk * ck[idx];   // residual in the rotated frame
+  const float r = yk - nk * s_ck[idx];   // residual in the rotated frame
   if (qp == 0) {
     s_r[j] = r;
     s_code[j] = idx;
@@ -141,7 +166,10 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
 #pragma unroll
     for (int cc = 0; cc < KQ; ++cc) {
       const int c = qp * KQ + cc;
-      pz = fmaf(spt[(size_t)c * M + j], s_r[c], pz);
+      float sv;
+      if constexpr (kColumnInRegs) sv = scol[cc];
+      else sv = spt[(size_t)c * M + j];
+      pz = fmaf(sv, s_r[c], pz);
     }
     __syncthreads();   // s_pa reads (y) done
     s_pa[qp][j] = pz;
