@@ -346,8 +346,10 @@ extern "C" int tq_ctx_set_decode_path(tq_ctx* ctx, int path) {
       if (ctx->bits == 0 || (ctx->d != 64 && ctx->d != 128 && ctx->d != 256)) return TQ_EUNSUPPORTED;
       break;
     case TQ_DECODE_TC:
-    case TQ_DECODE_TC4:
       if (ctx->d != 128 || (ctx->bits != 2 && ctx->bits != 3)) return TQ_EUNSUPPORTED;
+      break;
+    case TQ_DECODE_TC4:
+      if (ctx->d != 128 || ctx->bits < 2 || ctx->bits > 4) return TQ_EUNSUPPORTED;
       break;
     default:
       return TQ_EINVAL;

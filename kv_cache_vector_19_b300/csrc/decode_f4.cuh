@@ -202,7 +202,9 @@ __device__ __forceinline__ float piece_scale(float m) {
   return s;
 }
 
-template <int BITS, int GP, bool PAGED>
+// HSPLIT > 1: a.kv_heads counts virtual KV heads, HSPLIT per real one (each with a.group of its
+// query heads), and virtual KV head v reads the pages of real KV head v / HSPLIT.
+template <int BITS, int GP, bool PAGED, int HSPLIT>
 __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Params a, PageMap pm, float sparse_v) {
   using C = Cfg<BITS, GP>;
   using PL = typename C::PL;
@@ -320,7 +322,7 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
     const int p_lo = seg_lo, n_pages = max(0, min(seg_hi, valid_pages) - p_lo);
     const int slot = blockIdx.x - (seq * PM) / a.chunk;
     float* rec = a.part + ((size_t)seq * a.slots + slot) * G * (2 + D);
-    const uint8_t* seq_base = a.cache + (size_t)seq * PM * PL::bytes;
+    const uint8_t* seq_base = a.cache + (size_t)(seq / HSPLIT) * PM * PL::bytes;
     auto ring_slot = [&](int p) { return (pg_base + p) % NBUF; };
     auto ring_use = [&](int p) { return (pg_base + p) / NBUF; };
     auto pg_ptr = [&](int p) { return s_pages + ring_slot(p) * C::PAGE; };
@@ -339,7 +341,7 @@ __global__ void __launch_bounds__(Cfg<BITS, GP>::THREADS, 1) decode_f4_kernel(Pa
           if (lane == 0) atomicOr(a.status, kFlagBounds);
           blk = blk < 0 ? 0 : pm.n_blocks - 1;
         }
-        return a.cache + ((size_t)blk * a.kv_heads + kvh) * PL::bytes;
+        return a.cache + ((size_t)blk * (a.kv_heads / HSPLIT) + kvh / HSPLIT) * PL::bytes;
       } else {
         return seq_base + (size_t)(p_lo + i) * PL::bytes;
       }

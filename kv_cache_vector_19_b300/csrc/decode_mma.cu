@@ -321,23 +321,37 @@ int launch_decode_tc(const tq_ctx* c, const MmaPlan& pl, const float* q, int bat
 namespace tq {
 namespace {
 
-template <int BITS, int GP>
+template <int BITS, int GP, int SPLIT>
 int f4_prepare_one() {
   using C = dtf::Cfg<BITS, GP>;
   if constexpr (!C::SUPPORTED) {
     return TQ_OK;
   } else {
-    const bool ok = cudaFuncSetAttribute(dtf::decode_f4_kernel<BITS, GP, false>,
+    const bool ok = cudaFuncSetAttribute(dtf::decode_f4_kernel<BITS, GP, false, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) == cudaSuccess &&
-                    cudaFuncSetAttribute(dtf::decode_f4_kernel<BITS, GP, true>,
+                    cudaFuncSetAttribute(dtf::decode_f4_kernel<BITS, GP, true, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) == cudaSuccess;
     return ok ? TQ_OK : TQ_ECUDA;
   }
 }
 
-int f4_gp(int group) { return group <= 4 ? 4 : group <= 8 ? 8 : 0; }
+// Query heads of a KV head per kernel pass (gp, padded) and passes per KV head (split).  With
+// 4-bit codes the kernel's tensor memory holds two query heads, so a KV head with 4 or 8 runs as
+// 2 or 4 virtual KV heads of two query heads each, which read the same pages.
+struct F4Shape {
+  int gp, split;
+};
+F4Shape f4_shape(int bits, int group) {
+  if (bits == 4) {
+    if (group <= 2) return {2, 1};
+    if (group == 4) return {2, 2};
+    if (group == 8) return {2, 4};
+    return {0, 0};
+  }
+  return {group <= 4 ? 4 : group <= 8 ? 8 : 0, 1};
+}
 
-template <int BITS, int GP>
+template <int BITS, int GP, int SPLIT>
 int f4_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch, int q_heads, int kv_heads,
                   const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits, void* ws,
                   cudaStream_t st, const PageMap& pm) {
@@ -346,6 +360,7 @@ int f4_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
     return TQ_EUNSUPPORTED;
   } else {
     constexpr int D = 128;
+    const int kv_virtual = kv_heads * SPLIT;   // the plan is over the virtual KV heads
     float* qr = static_cast<float*>(ws);
     float* qs = qr + (size_t)batch * q_heads * D;
     float* part = qs + (size_t)batch * q_heads * D;
@@ -364,8 +379,8 @@ int f4_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
     a.asum_v = c->asum_v;
     a.batch = batch;
     a.q_heads = q_heads;
-    a.kv_heads = kv_heads;
-    a.group = q_heads / kv_heads;
+    a.kv_heads = kv_virtual;
+    a.group = q_heads / kv_virtual;
     a.max_tokens = max_tokens;
     a.pages_per_seq = pl.pages_per_seq;
     a.chunk = pl.chunk;
@@ -385,14 +400,15 @@ int f4_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = pm.table ? cudaLaunchKernelEx(&cfg, dtf::decode_f4_kernel<BITS, GP, true>, a, pm, c->sparse_v)
-                             : cudaLaunchKernelEx(&cfg, dtf::decode_f4_kernel<BITS, GP, false>, a, pm, c->sparse_v);
+    cudaError_t e =
+        pm.table ? cudaLaunchKernelEx(&cfg, dtf::decode_f4_kernel<BITS, GP, true, SPLIT>, a, pm, c->sparse_v)
+                 : cudaLaunchKernelEx(&cfg, dtf::decode_f4_kernel<BITS, GP, false, SPLIT>, a, pm, c->sparse_v);
     if (e != cudaSuccess) return TQ_ECUDA;
     cfg.gridDim = dim3(q_heads, batch);
     cfg.blockDim = dim3(4 * D);
     cfg.dynamicSmemBytes = 0;
     e = cudaLaunchKernelEx(&cfg, dmma::combine_kernel<D>, (const float*)part, (const float*)c->d_pi, out, q_heads,
-                           kv_heads, a.group, pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
+                           kv_virtual, a.group, pl.pages_per_seq, pl.chunk, pl.slots, pl.grid);
     return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
   }
 }
@@ -401,25 +417,27 @@ int f4_launch_one(const tq_ctx* c, const MmaPlan& pl, const float* q, int batch,
 
 bool decode_f4_supported(const tq_ctx* c, int q_heads, int kv_heads) {
   if (c->d != 128 || q_heads % kv_heads != 0) return false;
-  const int gp = f4_gp(q_heads / kv_heads);
-  if (gp == 0) return false;
+  const F4Shape sh = f4_shape(c->bits, q_heads / kv_heads);
+  if (sh.gp == 0) return false;
 #define TQ_S(BB, GG) \
-  if (c->bits == BB && gp == GG) return dtf::Cfg<BB, GG>::SUPPORTED;
-  TQ_S(2, 4) TQ_S(2, 8) TQ_S(3, 4) TQ_S(3, 8)
+  if (c->bits == BB && sh.gp == GG) return dtf::Cfg<BB, GG>::SUPPORTED;
+  TQ_S(2, 4) TQ_S(2, 8) TQ_S(3, 4) TQ_S(3, 8) TQ_S(4, 2)
 #undef TQ_S
   return false;
 }
 
 bool plan_decode_f4(const tq_ctx* c, int batch, int q_heads, int kv_heads, int max_tokens, MmaPlan* p) {
-  return decode_f4_supported(c, q_heads, kv_heads) && plan_pages(c->num_sms, batch, kv_heads, max_tokens, p);
+  if (!decode_f4_supported(c, q_heads, kv_heads)) return false;
+  const F4Shape sh = f4_shape(c->bits, q_heads / kv_heads);
+  return plan_pages(c->num_sms, batch, kv_heads * sh.split, max_tokens, p);
 }
 
 int prepare_decode_f4(const tq_ctx* c) {
   if (c->d != 128) return TQ_OK;
   int rc = TQ_OK;
-#define TQ_P(BB, GG) \
-  if (rc == TQ_OK && c->bits == BB) rc = f4_prepare_one<BB, GG>();
-  TQ_P(2, 4) TQ_P(2, 8) TQ_P(3, 4) TQ_P(3, 8)
+#define TQ_P(BB, GG, SS) \
+  if (rc == TQ_OK && c->bits == BB) rc = f4_prepare_one<BB, GG, SS>();
+  TQ_P(2, 4, 1) TQ_P(2, 8, 1) TQ_P(3, 4, 1) TQ_P(3, 8, 1) TQ_P(4, 2, 1) TQ_P(4, 2, 2) TQ_P(4, 2, 4)
 #undef TQ_P
   return rc;
 }
@@ -428,12 +446,12 @@ int launch_decode_f4(const tq_ctx* c, const MmaPlan& pl, const float* q, int bat
                      const void* cache, const int32_t* seq_lens, int max_tokens, float* out, float* logits_out,
                      void* workspace, void* stream, const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int gp = f4_gp(q_heads / kv_heads);
-#define TQ_L(BB, GG)                                                                                         \
-  if (c->bits == BB && gp == GG)                                                                             \
-    return f4_launch_one<BB, GG>(c, pl, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out, logits_out, \
-                                 workspace, st, pm);
-  TQ_L(2, 4) TQ_L(2, 8) TQ_L(3, 4) TQ_L(3, 8)
+  const F4Shape sh = f4_shape(c->bits, q_heads / kv_heads);
+#define TQ_L(BB, GG, SS)                                                                                       \
+  if (c->bits == BB && sh.gp == GG && sh.split == SS)                                                         \
+    return f4_launch_one<BB, GG, SS>(c, pl, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out,   \
+                                     logits_out, workspace, st, pm);
+  TQ_L(2, 4, 1) TQ_L(2, 8, 1) TQ_L(3, 4, 1) TQ_L(3, 8, 1) TQ_L(4, 2, 1) TQ_L(4, 2, 2) TQ_L(4, 2, 4)
 #undef TQ_L
   return TQ_EUNSUPPORTED;
 }

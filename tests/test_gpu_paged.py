@@ -106,7 +106,8 @@ DECODE_CASES = [
     dict(d=128, bits=3, G=4, path="auto"),     # e2m1 tcgen05
     dict(d=128, bits=3, G=8, path="auto"),     # e2m1 tcgen05, four token-warp sets
     dict(d=128, bits=2, G=16, path="auto"),    # f8f6f4 tcgen05
-    dict(d=128, bits=4, G=4, path="auto"),     # mma.sync
+    dict(d=128, bits=4, G=4, path="auto"),     # e2m1 tcgen05, two virtual KV heads per KV head
+    dict(d=128, bits=4, G=4, path="mma"),      # mma.sync
     dict(d=64, bits=3, G=2, path="auto"),
     dict(d=256, bits=3, G=4, path="simt"),     # CUDA cores
     dict(d=128, kv=(3, 4, True), G=4, path="auto"),   # format version 2

@@ -94,7 +94,9 @@ def test_decode_small(d, b, G):
     ("tc", 128, 3, 4), ("tc", 128, 3, 8), ("tc", 128, 3, 16), ("tc", 128, 2, 3), ("tc", 128, 2, 16),
     ("tc", 128, 3, 1), ("tc", 128, 3, 2), ("tc", 128, 3, 6), ("tc", 128, 2, 12),
     ("tc4", 128, 3, 4), ("tc4", 128, 3, 8), ("tc4", 128, 2, 3), ("tc4", 128, 3, 1), ("tc4", 128, 3, 2),
-    ("tc4", 128, 2, 8), ("tc4", 128, 3, 6), ("tc4", 128, 2, 5)])
+    ("tc4", 128, 2, 8), ("tc4", 128, 3, 6), ("tc4", 128, 2, 5),
+    # 4-bit codes: two query heads per pass, a KV head of 4 or 8 as 2 or 4 virtual ones
+    ("tc4", 128, 4, 1), ("tc4", 128, 4, 2), ("tc4", 128, 4, 4), ("tc4", 128, 4, 8)])
 def test_decode_small_each_kernel(path, d, b, G):
     _check_decode(d, b, G, path)
 
@@ -110,8 +112,8 @@ def test_decode_path_selection():
         assert ctx.workspace_bytes(2, 8, 2, 700) > 0
 
 
-@pytest.mark.parametrize("path,d,b", [("tc4", 128, 3), ("tc", 128, 3), ("mma", 128, 3), ("simt", 128, 3),
-                                      ("auto", 64, 3), ("auto", 256, 2)])
+@pytest.mark.parametrize("path,d,b", [("tc4", 128, 3), ("tc4", 128, 4), ("tc", 128, 3), ("mma", 128, 3),
+                                      ("simt", 128, 3), ("auto", 64, 3), ("auto", 256, 2)])
 def test_decode_long_sequences_each_kernel(path, d, b):
     """Sequences of ~120 pages, so that every CTA of the bit-plane kernels streams far more
     pages than its shared-memory ring holds (ring refills, many segments), checked on two

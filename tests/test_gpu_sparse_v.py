@@ -25,7 +25,8 @@ CASES = [
     dict(d=128, b=3, G=4, path="auto"),    # e2m1 tcgen05
     dict(d=128, b=3, G=8, path="auto"),    # e2m1 tcgen05, four token-warp sets
     dict(d=128, b=2, G=16, path="auto"),   # f8f6f4 tcgen05
-    dict(d=128, b=4, G=4, path="auto"),    # mma.sync
+    dict(d=128, b=4, G=4, path="auto"),    # e2m1 tcgen05, two virtual KV heads per KV head
+    dict(d=128, b=4, G=4, path="mma"),     # mma.sync
     dict(d=64, b=3, G=4, path="simt"),     # CUDA cores
 ]
 
