@@ -519,6 +519,9 @@ def run_case(args, w):
     if args.sparse_v:
         ctx.set_sparse_v(args.sparse_v)
     k, v = data["k"].cuda(), data["v"].cuda()
+    if args.token_major:   # a prefill projection's [B, T, H, d], quantized through strides
+        k = k.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+        v = v.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
     zero = torch.zeros(B, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
     if args.paged:   # a pool of blocks in a seeded random order, one table row per sequence
@@ -530,12 +533,18 @@ def run_case(args, w):
         T = 128 * max_blocks
 
         def quantize():
-            ctx.quantize_kv_paged(k, v, zero, cache, n_blocks, table)
+            if args.token_major:
+                ctx.quantize_kv_paged_strided(k, v, zero, cache, n_blocks, table)
+            else:
+                ctx.quantize_kv_paged(k, v, zero, cache, n_blocks, table)
     else:
         cache = ctx.alloc_cache(B, H, T)
 
         def quantize():
-            ctx.quantize_kv(k, v, zero, cache, T)
+            if args.token_major:
+                ctx.quantize_kv_strided(k, v, zero, cache, T)
+            else:
+                ctx.quantize_kv(k, v, zero, cache, T)
     if args.kernel_case == "quantize":
         call = quantize
     else:
@@ -579,6 +588,7 @@ def run_case(args, w):
     extra = (" (paged pool)" if args.paged else "") + (f" (sparse V {args.sparse_v:g})" if args.sparse_v else "")
     extra += (f" (queries x{args.q_scale:g})" if args.q_scale != 1.0 else "")
     extra += (f" ({args.decode_path} decode)" if args.decode_path != "auto" else "")
+    extra += (" (token-major K/V through strides)" if args.token_major else "")
     print(f"{args.kernel_case} case{extra}: {w.name}, {wl.tokens} tokens, "
           f"{args.warmup + args.steps} calls, status ok, "
           f"{ms * 1e3:.1f} us per call (back to back, cache {cache_mb:.0f} MB)", flush=True)
@@ -603,6 +613,8 @@ def main():
                     help="query scale of the kernel cases (larger: more peaked attention)")
     ap.add_argument("--decode-path", default="auto", choices=["auto", "simt", "mma", "tc", "tc4"],
                     help="decode kernel of the kernel cases")
+    ap.add_argument("--token-major", action="store_true",
+                    help="kernel cases: K/V stored [B, T, H, d] and quantized through strides")
     ap.add_argument("--paged", action="store_true",
                     help="--kernel-case quantize / decode on a block pool through a shuffled block table")
     args = ap.parse_args()

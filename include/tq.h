@@ -176,6 +176,19 @@ int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, int batch, i
                    int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
                    void* stream);
 
+/* tq_quantize_kv with the key and value vectors at any strides, so that a prefill writes its
+ * projection output straight into the compressed cache without a transpose ([3BITS]: the
+ * quantization overhead a prefill pays; [BLOG] 3.5, vLLM).  strides: host int64 [6], in bf16
+ * elements: element j of the key of token i of (batch b, kv head h) is
+ *   k[b * strides[0] + h * strides[1] + i * strides[2] + j]
+ * and likewise v with strides[3..5].  Each stride must be >= 0 and a multiple of 8 (rows stay
+ * on 16-byte boundaries); a [batch][n_tokens][kv_heads][d] projection output has
+ * (n_tokens kv_heads d, d, kv_heads d).  Otherwise exactly tq_quantize_kv (the contiguous
+ * call is strides (kv_heads n_tokens d, n_tokens d, d) twice); NULL strides: TQ_EINVAL. */
+int tq_quantize_kv_strided(const tq_ctx* ctx, const void* k, const void* v, const int64_t* strides,
+                           int batch, int kv_heads, int n_tokens, const int32_t* start_pos, void* cache,
+                           int max_tokens, void* stream);
+
 /* Scratch bytes tq_attn_decode needs for these sizes. */
 size_t tq_decode_workspace_bytes(const tq_ctx* ctx, int batch, int q_heads, int kv_heads,
                                  int max_tokens);
@@ -278,8 +291,9 @@ int tq_ctx_set_sparse_v(tq_ctx* ctx, float threshold);
  *   max_blocks   entries per table row; the sequences' capacity is max_blocks * 128 slots and
  *                takes the place of max_tokens in every other argument rule (start_pos,
  *                seq_lens, workspace: tq_decode_workspace_bytes(..., max_blocks * 128)).
- * Otherwise arguments, errors and results exactly as tq_quantize_kv, tq_attn_decode and
- * tq_dequantize_kv with `cache` replaced by (pool, n_blocks, block_table, max_blocks):
+ * Otherwise arguments, errors and results exactly as tq_quantize_kv, tq_attn_decode,
+ * tq_dequantize_kv and tq_ip_topk with `cache` replaced by (pool, n_blocks, block_table,
+ * max_blocks):
  * a paged pool whose table maps (b, p) to block b * max_blocks + p holds the contiguous
  * cache byte for byte when kv_heads == 1, and any table gives bit-identical outputs. */
 size_t tq_paged_pool_bytes(const tq_ctx* ctx, int kv_heads, int n_blocks);
@@ -293,6 +307,15 @@ int tq_attn_decode_paged(const tq_ctx* ctx, const float* q, int batch, int q_hea
 int tq_dequantize_kv_paged(const tq_ctx* ctx, const void* pool, int n_blocks, const int32_t* block_table,
                            int max_blocks, int batch, int kv_heads, const int32_t* start_pos, int n_tokens,
                            float* k_out, float* v_out, void* stream);
+/* tq_quantize_kv_paged with strided K / V (strides as tq_quantize_kv_strided). */
+int tq_quantize_kv_paged_strided(const tq_ctx* ctx, const void* k, const void* v, const int64_t* strides,
+                                 int batch, int kv_heads, int n_tokens, const int32_t* start_pos, void* pool,
+                                 int n_blocks, const int32_t* block_table, int max_blocks, void* stream);
+/* tq_ip_topk on a paged pool (workspace: tq_ip_topk_workspace_bytes(..., max_blocks * 128)). */
+int tq_ip_topk_paged(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                     const void* pool, int n_blocks, const int32_t* block_table, int max_blocks,
+                     const int32_t* seq_lens, int k, int32_t* out_idx, float* out_score, void* workspace,
+                     size_t workspace_bytes, void* stream);
 
 /* Self-test of the device-side failure path: launches one thread that waits, with the same
  * bounded wait every kernel uses, on an mbarrier nothing arrives at.  The wait gives up after

@@ -66,6 +66,12 @@ _SIGS = {
                                       _vp, _c_size, _vp]),
     "tq_dequantize_kv_paged": (_c_int, [_vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp,
                                         _vp]),
+    "tq_ip_topk_paged": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _c_int, _vp, _c_int, _vp,
+                                  _vp, _vp, _c_size, _vp]),
+    "tq_quantize_kv_strided": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(ctypes.c_int64), _c_int, _c_int, _c_int, _vp,
+                                        _vp, _c_int, _vp]),
+    "tq_quantize_kv_paged_strided": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(ctypes.c_int64), _c_int, _c_int, _c_int,
+                                              _vp, _vp, _c_int, _vp, _c_int, _vp]),
     "tq_selftest_bounded_wait": (_c_int, [_vp, _vp]),
     "tq_get_device_status": (_c_int, [_vp, _vp]),
     "tq_status_string": (ctypes.c_char_p, [_c_int]),
@@ -310,6 +316,29 @@ class Context:
                             _stream_handle(stream))
         _check("tq_attn_decode", rc)
 
+    @staticmethod
+    def _kv_strides(k, v):
+        """int64[6] element strides (batch, kv head, token) of k and v, viewed as [B, H, T, d]
+        with unit stride in d (a permuted view of a [B, T, H, d] projection output is fine)."""
+        if k.shape != v.shape or k.stride(3) != 1 or v.stride(3) != 1:
+            raise TQError("tq_quantize_kv_strided", TQ_EINVAL)
+        st = (ctypes.c_int64 * 6)(*(k.stride()[:3] + v.stride()[:3]))
+        return st
+
+    def quantize_kv_strided(self, k, v, start_pos, cache, max_tokens, stream=None):
+        """quantize_kv for k, v of logical shape [B, Hkv, n_tokens, d] with any strides (unit in d)."""
+        B, H, N, d = k.shape
+        rc = lib().tq_quantize_kv_strided(self._ctx, _ptr(k), _ptr(v), self._kv_strides(k, v), B, H, N,
+                                          _ptr(start_pos), _ptr(cache), max_tokens, _stream_handle(stream))
+        _check("tq_quantize_kv_strided", rc)
+
+    def quantize_kv_paged_strided(self, k, v, start_pos, pool, n_blocks, block_table, stream=None):
+        B, H, N, d = k.shape
+        rc = lib().tq_quantize_kv_paged_strided(self._ctx, _ptr(k), _ptr(v), self._kv_strides(k, v), B, H, N,
+                                                _ptr(start_pos), _ptr(pool), n_blocks, _ptr(block_table),
+                                                block_table.shape[1], _stream_handle(stream))
+        _check("tq_quantize_kv_paged_strided", rc)
+
     # ---- paged (block-table) cache: pool of blocks, each the kv_heads pages of 128 slots ----
     def alloc_pool(self, kv_heads, n_blocks):
         import torch
@@ -340,6 +369,25 @@ class Context:
                                           batch, kv_heads, _ptr(start_pos), n_tokens, _ptr(k_out), _ptr(v_out),
                                           _stream_handle(stream))
         _check("tq_dequantize_kv_paged", rc)
+
+    def ip_topk_paged(self, q, pool, n_blocks, block_table, seq_lens, kv_heads, k, out_idx=None, out_score=None,
+                      workspace=None, stream=None):
+        """ip_topk on a block pool (block_table int32 [B, max_blocks] on the device)."""
+        import torch
+        B, Hq, d = q.shape
+        T = 128 * block_table.shape[1]
+        if out_idx is None:
+            out_idx = torch.empty(B, Hq, k, dtype=torch.int32, device=q.device)
+        if out_score is None:
+            out_score = torch.empty(B, Hq, k, dtype=torch.float32, device=q.device)
+        if workspace is None:
+            workspace = self.alloc_topk_workspace(B, Hq, kv_heads, T)
+        rc = lib().tq_ip_topk_paged(self._ctx, _ptr(q), B, Hq, kv_heads, _ptr(pool), n_blocks, _ptr(block_table),
+                                    block_table.shape[1], _ptr(seq_lens), k, _ptr(out_idx), _ptr(out_score),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream_handle(stream))
+        _check("tq_ip_topk_paged", rc)
+        return out_idx, out_score
 
     def alloc_topk_workspace(self, batch, q_heads, kv_heads, max_tokens, device="cuda"):
         """Device scratch of tq_ip_topk (tq_ip_topk_workspace_bytes bytes)."""

@@ -283,7 +283,8 @@ extern "C" int tq_ctx_get_constants(const tq_ctx* ctx, double* pi, double* s, do
 namespace {
 
 int quantize_impl(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                  const int32_t* start_pos, void* cache, int max_tokens, const tq::PageMap& pm, void* stream) {
+                  const int32_t* start_pos, void* cache, int max_tokens, const tq::PageMap& pm,
+                  const int64_t* strides, void* stream) {
   if (!ctx) return TQ_EINVAL;
   if (batch < 1 || kv_heads < 1 || n_tokens < 0 || max_tokens < 1) return TQ_EINVAL;
   if (batch > 65535 || kv_heads > 65535) return TQ_EINVAL;
@@ -291,14 +292,23 @@ int quantize_impl(const tq_ctx* ctx, const void* k, const void* v, int batch, in
   if (n_tokens == 0) return TQ_OK;   // nothing to read or write; k and v may be NULL
   if (!k || !v || !start_pos || !cache) return TQ_EINVAL;
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(cache, 256) || !aligned(start_pos, 4)) return TQ_EINVAL;
+  tq::KVLayout lay = tq::contiguous_layout(kv_heads, n_tokens, ctx->d);
+  if (strides) {   // multiples of 8 elements keep every token's row on a 16-byte boundary
+    for (int i = 0; i < 6; ++i)
+      if (strides[i] < 0 || strides[i] % 8 != 0) return TQ_EINVAL;
+    lay = tq::KVLayout{strides[0], strides[1], strides[2], strides[3], strides[4], strides[5]};
+  }
   DeviceGuard guard(ctx->device);
   if (ctx->bits == 0)
-    return tq::launch_quantize_kv2(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream, pm);
+    return tq::launch_quantize_kv2(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, lay, stream,
+                                   pm);
   if (n_tokens <= tq::kFewTokens)
-    return tq::launch_quantize_few(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream, pm);
+    return tq::launch_quantize_few(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, lay, stream,
+                                   pm);
   if (ctx->d == 128)
-    return tq::launch_quantize_tc(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream, pm);
-  return launch_quantize_simt(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, stream, pm);
+    return tq::launch_quantize_tc(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, lay, stream,
+                                  pm);
+  return launch_quantize_simt(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, lay, stream, pm);
 }
 
 // The block-table arguments of the paged entry points: TQ_OK and the page map, or TQ_EINVAL.
@@ -318,7 +328,16 @@ int paged_map(const void* pool, int n_blocks, const int32_t* block_table, int ma
 extern "C" int tq_quantize_kv(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
                               int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
                               void* stream) {
-  return quantize_impl(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, tq::PageMap(), stream);
+  return quantize_impl(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, tq::PageMap(), nullptr,
+                       stream);
+}
+
+extern "C" int tq_quantize_kv_strided(const tq_ctx* ctx, const void* k, const void* v, const int64_t* strides,
+                                      int batch, int kv_heads, int n_tokens, const int32_t* start_pos, void* cache,
+                                      int max_tokens, void* stream) {
+  if (!strides) return TQ_EINVAL;
+  return quantize_impl(ctx, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, tq::PageMap(), strides,
+                       stream);
 }
 
 extern "C" size_t tq_paged_pool_bytes(const tq_ctx* ctx, int kv_heads, int n_blocks) {
@@ -333,7 +352,19 @@ extern "C" int tq_quantize_kv_paged(const tq_ctx* ctx, const void* k, const void
   int max_tokens = 0;
   const int rc = paged_map(pool, n_blocks, block_table, max_blocks, &pm, &max_tokens);
   if (rc != TQ_OK) return rc;
-  return quantize_impl(ctx, k, v, batch, kv_heads, n_tokens, start_pos, pool, max_tokens, pm, stream);
+  return quantize_impl(ctx, k, v, batch, kv_heads, n_tokens, start_pos, pool, max_tokens, pm, nullptr, stream);
+}
+
+extern "C" int tq_quantize_kv_paged_strided(const tq_ctx* ctx, const void* k, const void* v, const int64_t* strides,
+                                            int batch, int kv_heads, int n_tokens, const int32_t* start_pos,
+                                            void* pool, int n_blocks, const int32_t* block_table, int max_blocks,
+                                            void* stream) {
+  if (!strides) return TQ_EINVAL;
+  tq::PageMap pm;
+  int max_tokens = 0;
+  const int rc = paged_map(pool, n_blocks, block_table, max_blocks, &pm, &max_tokens);
+  if (rc != TQ_OK) return rc;
+  return quantize_impl(ctx, k, v, batch, kv_heads, n_tokens, start_pos, pool, max_tokens, pm, strides, stream);
 }
 
 extern "C" int tq_ctx_set_decode_path(tq_ctx* ctx, int path) {
@@ -494,9 +525,11 @@ extern "C" size_t tq_ip_topk_workspace_bytes(const tq_ctx* ctx, int batch, int q
   return align256(dw) + align256(rows * (size_t)max_tokens * 4) + align256(rows * (size_t)ctx->d * 4);
 }
 
-extern "C" int tq_ip_topk(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
-                          const void* cache, const int32_t* seq_lens, int max_tokens, int k, int32_t* out_idx,
-                          float* out_score, void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+int topk_impl(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
+              const int32_t* seq_lens, int max_tokens, int k, int32_t* out_idx, float* out_score, void* workspace,
+              size_t workspace_bytes, const tq::PageMap& pm, void* stream) {
   if (!ctx || k < 1 || k > TQ_TOPK_MAX || !out_idx || !out_score || !aligned(out_idx, 4) || !aligned(out_score, 4))
     return TQ_EINVAL;
   // the decode's own checks (out stands in for the decode output, which lives in the workspace)
@@ -512,10 +545,31 @@ extern "C" int tq_ip_topk(const tq_ctx* ctx, const float* q, int batch, int q_he
   uint8_t* w = static_cast<uint8_t*>(workspace);
   float* lg = reinterpret_cast<float*>(w + align256(dw));
   float* o = reinterpret_cast<float*>(w + align256(dw) + align256(rows * (size_t)max_tokens * 4));
-  const int rc = tq_attn_decode(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, o, lg, w, dw, stream);
+  const int rc = decode_impl(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, o, lg, w, dw, pm, stream);
   if (rc != TQ_OK) return rc;
   DeviceGuard guard(ctx->device);
   return tq::launch_topk(ctx, lg, seq_lens, batch, q_heads, max_tokens, k, out_idx, out_score, stream);
+}
+
+}  // namespace
+
+extern "C" int tq_ip_topk(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                          const void* cache, const int32_t* seq_lens, int max_tokens, int k, int32_t* out_idx,
+                          float* out_score, void* workspace, size_t workspace_bytes, void* stream) {
+  return topk_impl(ctx, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, k, out_idx, out_score, workspace,
+                   workspace_bytes, tq::PageMap(), stream);
+}
+
+extern "C" int tq_ip_topk_paged(const tq_ctx* ctx, const float* q, int batch, int q_heads, int kv_heads,
+                                const void* pool, int n_blocks, const int32_t* block_table, int max_blocks,
+                                const int32_t* seq_lens, int k, int32_t* out_idx, float* out_score, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  tq::PageMap pm;
+  int max_tokens = 0;
+  const int rc = paged_map(pool, n_blocks, block_table, max_blocks, &pm, &max_tokens);
+  if (rc != TQ_OK) return rc;
+  return topk_impl(ctx, q, batch, q_heads, kv_heads, pool, seq_lens, max_tokens, k, out_idx, out_score, workspace,
+                   workspace_bytes, pm, stream);
 }
 
 namespace {

@@ -68,6 +68,7 @@ struct QArgs {
   const float* exact;
   int* status;
   PageMap pm;
+  KVLayout lay;         // element strides of k and v over (batch, KV head, token)
   Geom g;
 };
 
@@ -113,7 +114,7 @@ __device__ __forceinline__ void gemm64(const float* __restrict__ A, const float*
 // Loads 64 bf16 rows (slots s0 .. s0+63 of the page) into fp32 rows of xs; rows outside
 // [lo, hi) are zero.  Then one warp per row computes the fp32 norm.
 template <int D>
-__device__ __forceinline__ void load_rows(const __nv_bfloat16* __restrict__ src_seq, int page, int start, int s0,
+__device__ __forceinline__ void load_rows(const __nv_bfloat16* __restrict__ src_seq, int64_t ts, int page, int start, int s0,
                                           int lo, int hi, float* xs, float* nrm) {
   const int tid = threadIdx.x;
   for (int e = tid; e < kRows * (D / 8); e += kThreads) {
@@ -122,7 +123,7 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16* __restrict__ src_
     float f[8];
     if (slot >= lo && slot < hi) {
       const long tok = (long)page * 128 + slot - start;
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src_seq + tok * D) + ch);
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src_seq + tok * ts) + ch);
       const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -155,14 +156,14 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16* __restrict__ src_
 // exactly; returns this thread's (possibly new) code.
 template <int D>
 __device__ __forceinline__ int resolve_codes(bool near, int idx, int row, int j, const __nv_bfloat16* src_seq,
-                                             int page, int start, int s0, const float* pih, const float* pil,
+                                             int64_t ts, int page, int start, int s0, const float* pih, const float* pil,
                                              const float* th, const float* tl, int nb, int lane) {
   uint32_t ev = __ballot_sync(0xffffffffu, near);
   while (ev) {
     const int L = __ffs(ev) - 1;
     ev &= ev - 1;
     const int rowL = __shfl_sync(0xffffffffu, row, L), jL = __shfl_sync(0xffffffffu, j, L);
-    const int r = exact::code_of_row<D>(src_seq + ((long)page * 128 + s0 + rowL - start) * D, pih, pil, jL, th, tl,
+    const int r = exact::code_of_row<D>(src_seq + ((long)page * 128 + s0 + rowL - start) * ts, pih, pil, jL, th, tl,
                                         nb, lane);
     if (lane == L) idx = r;
   }
@@ -225,15 +226,15 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QArgs a) {
   float* g_gm = reinterpret_cast<float*>(pg + g.off_gamma);
   uint32_t* g_vc = reinterpret_cast<uint32_t*>(pg + g.off_vcodes);
   float* g_nv = reinterpret_cast<float*>(pg + g.off_nv);
-  const __nv_bfloat16* kseq = a.k + seq * (size_t)a.n_tokens * D;
-  const __nv_bfloat16* vseq = a.v + seq * (size_t)a.n_tokens * D;
+  const __nv_bfloat16* kseq = a.k + (b * a.lay.kb + h * a.lay.kh);   // token i at kseq + i kt
+  const __nv_bfloat16* vseq = a.v + (b * a.lay.vb + h * a.lay.vh);
   __syncthreads();
 
   for (int half = 0; half < 2; ++half) {
     const int s0 = half * kRows;
     if (hi <= s0 || lo >= s0 + kRows) continue;
     // ---------------- keys ----------------
-    load_rows<D>(kseq, page, start, s0, lo, hi, xs, nrm);
+    load_rows<D>(kseq, a.lay.kt, page, start, s0, lo, hi, xs, nrm);
     gemm64<D, D>(xs, a.pit, ys);
     __syncthreads();
     for (int e = tid; e < kRows * D; e += kThreads) {
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QArgs a) {
       const float yh = n > 0.f ? y / n : 0.f;
       bool near;
       int idx = fast_code(yh, s_tk, LK - 1, s_nk, near);
-      idx = resolve_codes<D>(near && n > 0.f, idx, row, j, kseq, page, start, s0, T.pih, T.pil, T.tkh, T.tkl, LK - 1,
+      idx = resolve_codes<D>(near && n > 0.f, idx, row, j, kseq, a.lay.kt, page, start, s0, T.pih, T.pil, T.tkh, T.tkl, LK - 1,
                              lane);
       kcode[row * D + j] = (uint8_t)idx;
       ys[row * (D + 1) + j] = y - n * s_ck[idx];   // r_rot = Pi r
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QArgs a) {
           int codes[D / 32];
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) codes[q] = kcode[rowL * D + lane * (D / 32) + q];
-          const bool sg = exact::sign_of_row<D>(kseq + ((long)page * 128 + s0 + rowL - start) * D, codes, T.sh, T.sl,
+          const bool sg = exact::sign_of_row<D>(kseq + ((long)page * 128 + s0 + rowL - start) * a.lay.kt, codes, T.sh, T.sl,
                                                 T.qh, T.ql, T.ckh, T.ckl, iL, lane);
           if (lane == L) xs[row * (D + 1) + i] = sg ? 1.f : -1.f;
         }
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QArgs a) {
     }
     __syncthreads();
     // ---------------- values ----------------
-    load_rows<D>(vseq, page, start, s0, lo, hi, xs, nrm);
+    load_rows<D>(vseq, a.lay.vt, page, start, s0, lo, hi, xs, nrm);
     gemm64<D, D>(xs, a.pit, ys);
     __syncthreads();
     for (int e = tid; e < kRows * D; e += kThreads) {
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(QArgs a) {
       const float yh = n > 0.f ? ys[row * (D + 1) + j] / n : 0.f;
       bool near;
       int idx = fast_code(yh, s_tv, LV - 1, s_nv, near);
-      idx = resolve_codes<D>(near && n > 0.f, idx, row, j, vseq, page, start, s0, T.pih, T.pil, T.tvh, T.tvl, LV - 1,
+      idx = resolve_codes<D>(near && n > 0.f, idx, row, j, vseq, a.lay.vt, page, start, s0, T.pih, T.pil, T.tvh, T.tvl, LV - 1,
                              lane);
       vcode[(s0 + row) * D + j] = (uint8_t)idx;
     }
@@ -359,7 +360,8 @@ constexpr size_t quant_smem_bytes() {
 
 template <int D>
 int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-             const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm) {
+             const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm,
+             const KVLayout& lay) {
   QArgs a;
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
@@ -378,6 +380,7 @@ int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_he
   a.exact = c->d_exact;
   a.status = c->d_status;
   a.pm = pm;
+  a.lay = lay;
   a.g = geom_of(c);
   const dim3 grid((n_tokens + 127) / 128 + 1, kv_heads, batch);
   quantize_kernel<D><<<grid, kThreads, quant_smem_bytes<D>(), st>>>(a);
@@ -756,11 +759,12 @@ int prepare_kv2(const tq_ctx* c) {
 }
 
 int launch_quantize_kv2(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                        const int32_t* start_pos, void* cache, int max_tokens, void* stream, const PageMap& pm) {
+                        const int32_t* start_pos, void* cache, int max_tokens, const KVLayout& lay, void* stream,
+                        const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (c->d == 64) return kv2::launch_q<64>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
-  if (c->d == 128) return kv2::launch_q<128>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
-  if (c->d == 256) return kv2::launch_q<256>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
+  if (c->d == 64) return kv2::launch_q<64>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm, lay);
+  if (c->d == 128) return kv2::launch_q<128>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm, lay);
+  if (c->d == 256) return kv2::launch_q<256>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm, lay);
   return TQ_EUNSUPPORTED;
 }
 

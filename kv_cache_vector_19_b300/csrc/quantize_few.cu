@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
                                                          const float* __restrict__ ck, const float* __restrict__ tk,
                                                          const float* __restrict__ cv, const float* __restrict__ tv,
                                                          const float* __restrict__ exact_tabs, int* status,
-                                                         PageMap pm) {
+                                                         PageMap pm, KVLayout lay) {
   using PL = PageLayout<D, BITS>;
   constexpr int M = D, BK = BITS - 1, BV = BITS, LK = 1 << BK, LV = 1 << BV;
   constexpr int NT = 4 * D, KQ = D / 4;   // 4 D threads: coordinate j, quarter qp of each sum
@@ -85,11 +85,13 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
   }
   const int pos = start + t, page = pos >> 7, slot = pos & 127;
   uint8_t* pg = cache + pm.index(seq, kv_heads, pages_per_seq, page, status) * PL::bytes;
-  const size_t row = ((size_t)seq * n_tokens + t) * D;
+  const int hkv = seq - b * kv_heads;
+  const size_t krow = (size_t)(b * lay.kb + hkv * lay.kh + t * lay.kt);   // this token's key row
+  const size_t vrow = (size_t)(b * lay.vb + hkv * lay.vh + t * lay.vt);
   float xk = 0.f, xv = 0.f;
   if (qp == 0) {
-    xk = __bfloat162float(k[row + j]);
-    xv = __bfloat162float(v[row + j]);
+    xk = __bfloat162float(k[krow + j]);
+    xv = __bfloat162float(v[vrow + j]);
     s_xk[j] = xk;
     s_xv[j] = xv;
     if (j < BK * PL::KW + PL::SW) s_words[j] = 0u;
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
     uint32_t ev = __ballot_sync(0xffffffffu, nk_near);
     if (ev) {
       float x[D / 32];
-      exact::load_row<D>(k + row, lane, x);
+      exact::load_row<D>(k + krow, lane, x);
       const exact::F2 n = exact::norm<D>(x);
       while (ev) {
         const int L = __ffs(ev) - 1;
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
     ev = __ballot_sync(0xffffffffu, nv_near);
     if (ev) {
       float x[D / 32];
-      exact::load_row<D>(v + row, lane, x);
+      exact::load_row<D>(v + vrow, lane, x);
       const exact::F2 n = exact::norm<D>(x);
       while (ev) {
         const int L = __ffs(ev) - 1;
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
     if (ev) {
       float x[D / 32];
       int codes[D / 32];
-      exact::load_row<D>(k + row, lane, x);
+      exact::load_row<D>(k + krow, lane, x);
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) codes[q] = s_code[lane * (D / 32) + q];
       const exact::F2 n = exact::norm<D>(x);
@@ -228,23 +230,25 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
 
 template <int D, int BITS>
 int launch_one(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-               const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm) {
+               const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm,
+               const KVLayout& lay) {
   const dim3 grid((unsigned)n_tokens, (unsigned)(batch * kv_heads));
   quantize_few_kernel<D, BITS><<<grid, 4 * D, 0, st>>>(
       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), kv_heads, n_tokens, max_tokens,
       (max_tokens + 127) / 128, start_pos, static_cast<uint8_t*>(cache), c->d_pit, c->d_spt, c->d_ck, c->d_tk,
-      c->d_cv, c->d_tv, c->d_exact, c->d_status, pm);
+      c->d_cv, c->d_tv, c->d_exact, c->d_status, pm, lay);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
 }
 
 }  // namespace
 
 int launch_quantize_few(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                        const int32_t* start_pos, void* cache, int max_tokens, void* stream, const PageMap& pm) {
+                        const int32_t* start_pos, void* cache, int max_tokens, const KVLayout& lay, void* stream,
+                        const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define TQ_QF(DD, BB) \
   if (c->d == DD && c->bits == BB) \
-    return launch_one<DD, BB>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
+    return launch_one<DD, BB>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm, lay);
   TQ_QF(64, 2) TQ_QF(64, 3) TQ_QF(64, 4) TQ_QF(64, 5) TQ_QF(128, 2) TQ_QF(128, 3) TQ_QF(128, 4) TQ_QF(128, 5)
   TQ_QF(256, 2) TQ_QF(256, 3) TQ_QF(256, 4) TQ_QF(256, 5)
 #undef TQ_QF

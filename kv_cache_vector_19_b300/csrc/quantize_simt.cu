@@ -39,6 +39,7 @@ struct QArgs {
   const float* exact;   // exact-decision tables
   int* status;
   PageMap pm;
+  KVLayout lay;         // element strides of k and v over (batch, KV head, token)
 };
 
 // C[64][N] (row stride N+1) = A[64][D] (row stride D+1) * Bt[D][N]; 256 threads,
@@ -83,7 +84,7 @@ __device__ __forceinline__ void gemm64(const float* __restrict__ A, const float*
 // Loads up to 64 bf16 rows (slots s0 .. s0+63 of the page) into fp32 smem; rows outside
 // [lo, hi) are zero.  Then one warp per row computes the fp32 norm.
 template <int D>
-__device__ __forceinline__ void load_rows(const __nv_bfloat16* __restrict__ src_seq, int page, int start,
+__device__ __forceinline__ void load_rows(const __nv_bfloat16* __restrict__ src_seq, int64_t ts, int page, int start,
                                           int s0, int lo, int hi, float* xs, float* nrm) {
   const int tid = threadIdx.x;
   for (int e = tid; e < kRows * (D / 8); e += kThreads) {
@@ -92,7 +93,7 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16* __restrict__ src_
     float f[8];
     if (slot >= lo && slot < hi) {
       long tok = (long)page * 128 + slot - start;
-      uint4 raw = __ldg(reinterpret_cast<const uint4*>(src_seq + tok * D) + ch);
+      uint4 raw = __ldg(reinterpret_cast<const uint4*>(src_seq + tok * ts) + ch);
       const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&raw);
 #pragma unroll
       for (int u = 0; u < 8; ++u) f[u] = __bfloat162float(hv[u]);
@@ -131,7 +132,7 @@ __device__ __forceinline__ int encode(float yhat, const float* t) {
 // boundary, taken again exactly (exact.cuh); returns this thread's (possibly new) code.
 template <int D>
 __device__ __forceinline__ int resolve_codes(bool near, int idx, int row, int j, const __nv_bfloat16* src_seq,
-                                             int page, int start, int s0, const float* th, const float* tl, int nb,
+                                             int64_t ts, int page, int start, int s0, const float* th, const float* tl, int nb,
                                              const exact::Tables& T, int lane) {
   uint32_t ev = __ballot_sync(0xffffffffu, near);
   while (ev) {
@@ -139,7 +140,7 @@ __device__ __forceinline__ int resolve_codes(bool near, int idx, int row, int j,
     ev &= ev - 1;
     const int rowL = __shfl_sync(0xffffffffu, row, L), jL = __shfl_sync(0xffffffffu, j, L);
     float x[D / 32];
-    exact::load_row<D>(src_seq + ((long)page * 128 + s0 + rowL - start) * D, lane, x);
+    exact::load_row<D>(src_seq + ((long)page * 128 + s0 + rowL - start) * ts, lane, x);
     const exact::F2 n = exact::norm<D>(x);
     const int r = exact::code<D>(x, n, T.pih, T.pil, jL, th, tl, nb, lane);
     if (lane == L) idx = r;
@@ -194,15 +195,15 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
   float* g_gm = reinterpret_cast<float*>(pg + PL::off_gamma);
   uint32_t* g_vc = reinterpret_cast<uint32_t*>(pg + PL::off_vcodes);
   float* g_nv = reinterpret_cast<float*>(pg + PL::off_nv);
-  const __nv_bfloat16* kseq = a.k + seq * (size_t)a.n_tokens * D;
-  const __nv_bfloat16* vseq = a.v + seq * (size_t)a.n_tokens * D;
+  const __nv_bfloat16* kseq = a.k + (b * a.lay.kb + h * a.lay.kh);   // token i at kseq + i kt
+  const __nv_bfloat16* vseq = a.v + (b * a.lay.vb + h * a.lay.vh);
   __syncthreads();
 
   for (int half = 0; half < 2; ++half) {
     const int s0 = half * kRows;
     if (hi <= s0 || lo >= s0 + kRows) continue;
     // ---------------- keys ----------------
-    load_rows<D>(kseq, page, start, s0, lo, hi, xs, nrm);
+    load_rows<D>(kseq, a.lay.kt, page, start, s0, lo, hi, xs, nrm);
     gemm64<D, D>(xs, a.pit, ys);
     __syncthreads();
     for (int e = tid; e < kRows * D; e += kThreads) {
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
       float yh = n > 0.f ? y / n : 0.f;
       int idx = encode<LK>(yh, s_tk);
       const bool near = n > 0.f && fabsf(yh - s_nk[idx].x) > s_nk[idx].y;
-      idx = resolve_codes<D>(near, idx, row, j, kseq, page, start, s0, T.tkh, T.tkl, LK - 1, T, lane);
+      idx = resolve_codes<D>(near, idx, row, j, kseq, a.lay.kt, page, start, s0, T.tkh, T.tkl, LK - 1, T, lane);
       kcode[row * D + j] = (uint8_t)idx;
       ys[row * (D + 1) + j] = y - n * s_ck[idx];                   // r_rot = Pi r
     }
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
         const int rowL = __shfl_sync(0xffffffffu, row, L), iL = __shfl_sync(0xffffffffu, i, L);
         float x[D / 32];
         int codes[D / 32];
-        exact::load_row<D>(kseq + ((long)page * 128 + s0 + rowL - start) * D, lane, x);
+        exact::load_row<D>(kseq + ((long)page * 128 + s0 + rowL - start) * a.lay.kt, lane, x);
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) codes[q] = kcode[rowL * D + lane * (D / 32) + q];
         const exact::F2 n = exact::norm<D>(x);
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
     }
     __syncthreads();
     // ---------------- values ----------------
-    load_rows<D>(vseq, page, start, s0, lo, hi, xs, nrm);
+    load_rows<D>(vseq, a.lay.vt, page, start, s0, lo, hi, xs, nrm);
     gemm64<D, D>(xs, a.pit, ys);
     __syncthreads();
     for (int e = tid; e < kRows * D; e += kThreads) {
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) quantize_simt_kernel(QArgs a) {
       float yh = n > 0.f ? ys[row * (D + 1) + j] / n : 0.f;
       int idx = encode<LV>(yh, s_tv);
       const bool near = n > 0.f && fabsf(yh - s_nv[idx].x) > s_nv[idx].y;
-      idx = resolve_codes<D>(near, idx, row, j, vseq, page, start, s0, T.tvh, T.tvl, LV - 1, T, lane);
+      idx = resolve_codes<D>(near, idx, row, j, vseq, a.lay.vt, page, start, s0, T.tvh, T.tvl, LV - 1, T, lane);
       vcode[(s0 + row) * D + j] = (uint8_t)idx;
     }
     for (int row = tid; row < kRows; row += kThreads) {
@@ -338,7 +339,8 @@ int prepare_q() {
 
 template <int D, int BITS>
 int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-             const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm) {
+             const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm,
+             const KVLayout& lay) {
   constexpr size_t smem = quant_smem_bytes<D>();
   QArgs a;
   a.k = static_cast<const __nv_bfloat16*>(k);
@@ -358,6 +360,7 @@ int launch_q(const tq_ctx* c, const void* k, const void* v, int batch, int kv_he
   a.exact = c->d_exact;
   a.status = c->d_status;
   a.pm = pm;
+  a.lay = lay;
   dim3 grid((n_tokens + 127) / 128 + 1, kv_heads, batch);
   quantize_simt_kernel<D, BITS><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
@@ -378,11 +381,11 @@ int prepare_quantize_simt(const tq_ctx* c) {
 
 int launch_quantize_simt(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads,
                          int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
-                         void* stream, const tq::PageMap& pm) {
+                         const tq::KVLayout& lay, void* stream, const tq::PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define TQ_Q(DD, BB)                                                                              \
   if (c->d == DD && c->bits == BB)                                                                \
-    return tq::launch_q<DD, BB>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
+    return tq::launch_q<DD, BB>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm, lay);
   TQ_Q(64, 2) TQ_Q(64, 3) TQ_Q(64, 4) TQ_Q(64, 5)
   TQ_Q(128, 2) TQ_Q(128, 3) TQ_Q(128, 4) TQ_Q(128, 5)
   TQ_Q(256, 2) TQ_Q(256, 3) TQ_Q(256, 4) TQ_Q(256, 5)

@@ -73,6 +73,7 @@ struct QArgs {
   const float* tv;
   int* status;
   PageMap pm;
+  KVLayout lay;          // element strides of k and v over (batch, KV head, token)
 };
 
 __device__ __forceinline__ float bf16_val(uint32_t bits) { return __uint_as_float(bits << 16); }
@@ -173,25 +174,38 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
     const int hi = min(start + a.n_tokens, page * 128 + 128) - page * 128;
     if (lo >= hi) continue;
     uint8_t* pg = a.cache + a.pm.index(seq, a.kv_heads, a.pages_per_seq, page, a.status) * PL::bytes;
-    const __nv_bfloat16* kseq = a.k + (size_t)seq * a.n_tokens * D;
-    const __nv_bfloat16* vseq = a.v + (size_t)seq * a.n_tokens * D;
+    const int hkv = seq - b * a.kv_heads;
+    const __nv_bfloat16* kseq = a.k + (b * a.lay.kb + hkv * a.lay.kh);   // token i at kseq + i kt
+    const __nv_bfloat16* vseq = a.v + (b * a.lay.vb + hkv * a.lay.vh);
 
     // ---- stage K and V rows (slots outside [lo, hi) are zero); row norms on the way ----
     __syncthreads();   // previous item done with sK / sV
     if (*s_fail) break;   // uniform: a bounded wait gave up
-    if (tid == 0) {
-      // the rows of this CTA's next item into L2 while this one is processed
+    if (warp == 0) {
+      // the rows of this CTA's next item into L2 while this one is processed: one range when
+      // the rows are contiguous, else row by row over the lanes
       const int nx = item + (int)gridDim.x;
       if (nx < n_items) {
         const int nip = nx % a.items_per_seq, nseq = nx / a.items_per_seq;
-        const int nstart = a.start_pos[nseq / a.kv_heads];
+        const int nb = nseq / a.kv_heads, nh = nseq - nb * a.kv_heads;
+        const int nstart = a.start_pos[nb];
         if (nstart >= 0 && nstart <= a.max_tokens - a.n_tokens) {
           const int npage = nstart / 128 + nip;
           const int nlo = max(nstart, npage * 128), nhi = min(nstart + a.n_tokens, npage * 128 + 128);
           if (nlo < nhi) {
-            const size_t off = ((size_t)nseq * a.n_tokens + (size_t)(nlo - nstart)) * D;
-            prefetch_l2(a.k + off, (uint32_t)(nhi - nlo) * D * 2);
-            prefetch_l2(a.v + off, (uint32_t)(nhi - nlo) * D * 2);
+            const __nv_bfloat16* nk = a.k + (nb * a.lay.kb + nh * a.lay.kh + (nlo - nstart) * a.lay.kt);
+            const __nv_bfloat16* nv = a.v + (nb * a.lay.vb + nh * a.lay.vh + (nlo - nstart) * a.lay.vt);
+            if (a.lay.kt == D && a.lay.vt == D) {
+              if (lane == 0) {
+                prefetch_l2(nk, (uint32_t)(nhi - nlo) * D * 2);
+                prefetch_l2(nv, (uint32_t)(nhi - nlo) * D * 2);
+              }
+            } else {
+              for (int r = lane; r < nhi - nlo; r += 32) {
+                prefetch_l2(nk + r * a.lay.kt, D * 2);
+                prefetch_l2(nv + r * a.lay.vt, D * 2);
+              }
+            }
           }
         }
       }
@@ -205,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
       for (int grp = warp; grp < 16; grp += 8) {
         const int r = 8 * grp + s8, vs = slot_of(r >> 5, r & 31);
         const bool kval = r >= lo && r < hi, vval = vs >= lo && vs < hi;
-        const uint4* kp = reinterpret_cast<const uint4*>(kseq + ((long)page * 128 + r - start) * D);
-        const uint4* vp = reinterpret_cast<const uint4*>(vseq + ((long)page * 128 + vs - start) * D);
+        const uint4* kp = reinterpret_cast<const uint4*>(kseq + ((long)page * 128 + r - start) * a.lay.kt);
+        const uint4* vp = reinterpret_cast<const uint4*>(vseq + ((long)page * 128 + vs - start) * a.lay.vt);
         uint4 xk[4], xv[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -332,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
             const int L = __ffs(lanes) - 1;
             lanes &= lanes - 1;
             uint32_t m = __shfl_sync(0xffffffffu, near, L);
-            const __nv_bfloat16* xr = kseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * D;
+            const __nv_bfloat16* xr = kseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * a.lay.kt;
             while (m) {
               const int j = c0 + __ffs(m) - 1;
               m &= m - 1;
@@ -413,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
           const int L = __ffs(lanes) - 1;
           lanes &= lanes - 1;
           uint32_t m = __shfl_sync(0xffffffffu, near, L);
-          const __nv_bfloat16* xr = vseq + ((long)page * 128 + __shfl_sync(0xffffffffu, slot, L) - start) * D;
+          const __nv_bfloat16* xr = vseq + ((long)page * 128 + __shfl_sync(0xffffffffu, slot, L) - start) * a.lay.vt;
           while (m) {
             const int cc = __ffs(m) - 1;
             m &= m - 1;
@@ -489,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) codes[e] |= (int)((kw >> kbit(4 * lane + e)) & 1u) << q;
           }
-          const __nv_bfloat16* xr = kseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * D;
+          const __nv_bfloat16* xr = kseq + ((long)page * 128 + 32 * (warp & 3) + L - start) * a.lay.kt;
           while (m) {
             const int i = c0 + __ffs(m) - 1;
             m &= m - 1;
@@ -534,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_tc_kernel(QArgs a) {
 
 template <int BITS>
 int launch(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-           const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm) {
+           const int32_t* start_pos, void* cache, int max_tokens, cudaStream_t st, const PageMap& pm,
+           const KVLayout& lay) {
   QArgs a;
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
@@ -554,6 +569,7 @@ int launch(const tq_ctx* c, const void* k, const void* v, int batch, int kv_head
   a.tv = c->d_tv;
   a.status = c->d_status;
   a.pm = pm;
+  a.lay = lay;
   const long items = (long)batch * kv_heads * a.items_per_seq;
   const int grid = (int)(items < c->num_sms ? items : c->num_sms);
   quantize_tc_kernel<BITS><<<grid, kThreads, SMEM, st>>>(a);
@@ -576,14 +592,15 @@ int prepare_quantize_tc(const tq_ctx* c) {
 }
 
 int launch_quantize_tc(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                       const int32_t* start_pos, void* cache, int max_tokens, void* stream, const PageMap& pm) {
+                       const int32_t* start_pos, void* cache, int max_tokens, const KVLayout& lay, void* stream,
+                       const PageMap& pm) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->d != 128 || !c->d_qblob) return TQ_EUNSUPPORTED;
   switch (c->bits) {
-    case 2: return qtc::launch<2>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
-    case 3: return qtc::launch<3>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
-    case 4: return qtc::launch<4>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
-    case 5: return qtc::launch<5>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm);
+    case 2: return qtc::launch<2>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm, lay);
+    case 3: return qtc::launch<3>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm, lay);
+    case 4: return qtc::launch<4>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm, lay);
+    case 5: return qtc::launch<5>(c, k, v, batch, kv_heads, n_tokens, start_pos, cache, max_tokens, st, pm, lay);
     default: return TQ_EUNSUPPORTED;
   }
 }

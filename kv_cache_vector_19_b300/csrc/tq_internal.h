@@ -58,6 +58,18 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 #endif
 
+// Element strides of the bf16 K and V inputs of a quantize call over (batch, KV head, token);
+// the d values of one token are contiguous.  The contiguous [batch][kv_heads][n_tokens][d]
+// layout is (H T d, T d, d); a prefill projection's [batch][n_tokens][kv_heads][d] is
+// (T H d, d, H d).
+struct KVLayout {
+  int64_t kb, kh, kt, vb, vh, vt;
+};
+inline KVLayout contiguous_layout(int kv_heads, int n_tokens, int d) {
+  const int64_t t = d, h = (int64_t)n_tokens * d, b = (int64_t)kv_heads * n_tokens * d;
+  return KVLayout{b, h, t, b, h, t};
+}
+
 // Decode split plan shared by the workspace query and the launch.
 struct SplitPlan {
   int pages, splits, pages_per_split;
@@ -117,17 +129,17 @@ int launch_dequantize(const tq_ctx* c, const void* cache, int batch, int kv_head
 // Few tokens per sequence (appends): one CTA per new vector pair.
 constexpr int kFewTokens = 8;
 int launch_quantize_few(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                        const int32_t* start_pos, void* cache, int max_tokens, void* stream,
+                        const int32_t* start_pos, void* cache, int max_tokens, const KVLayout& lay, void* stream,
     const PageMap& pm = PageMap());
 int launch_quantize_tc(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                       const int32_t* start_pos, void* cache, int max_tokens, void* stream,
+                       const int32_t* start_pos, void* cache, int max_tokens, const KVLayout& lay, void* stream,
     const PageMap& pm = PageMap());
 }  // namespace tq
 
 // Kernel launchers (return TQ_OK or TQ_ECUDA).
 int launch_quantize_simt(const tq_ctx* ctx, const void* k, const void* v, int batch, int kv_heads,
                          int n_tokens, const int32_t* start_pos, void* cache, int max_tokens,
-                         void* stream,
+                         const tq::KVLayout& lay, void* stream,
     const tq::PageMap& pm = tq::PageMap());
 namespace tq {
 int prepare_decode_mma(const tq_ctx* c);
@@ -177,7 +189,7 @@ int launch_topk(const tq_ctx* c, const float* logits, const int32_t* seq_lens, i
 // counts and m read from the context.
 int prepare_kv2(const tq_ctx* c);
 int launch_quantize_kv2(const tq_ctx* c, const void* k, const void* v, int batch, int kv_heads, int n_tokens,
-                        const int32_t* start_pos, void* cache, int max_tokens, void* stream,
+                        const int32_t* start_pos, void* cache, int max_tokens, const KVLayout& lay, void* stream,
     const PageMap& pm = PageMap());
 int launch_decode_kv2(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_heads, const void* cache,
                       const int32_t* seq_lens, int max_tokens, float* out, float* logits_out, void* workspace,

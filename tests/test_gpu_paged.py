@@ -11,7 +11,7 @@ to the oracle:
 * decode outputs and logits are bit-identical to the contiguous decode for every decode kernel
   (e2m1 and f8f6f4 tcgen05, mma.sync, CUDA cores, format version 2), and within the bars of
   the oracle's route A on the gathered pages;
-* dequantized vectors are bit-identical;
+* dequantized vectors and the scan's top-k are bit-identical;
 * a block id outside the pool is clamped and reported as TQ_EBOUNDS; bad table arguments are
   rejected on the host.
 """
@@ -177,6 +177,19 @@ def test_paged_dequantize_equals_contiguous():
     pr.ctx.dequantize_kv_paged(pr.pool, pr.n_blocks, pr.table, st, B, H, 200, k_out=kp, v_out=vp)
     assert pr.status() == tq.TQ_OK
     assert torch.equal(kc, kp) and torch.equal(vc, vp)
+
+
+def test_paged_scan_equals_contiguous():
+    d, B, H, G, max_blocks = 128, 2, 2, 4, 4
+    pr = Pair(d, B, H, max_blocks, bits=3, seed=4)
+    k, v = _kv(B, H, pr.T, d, 12)
+    pr.quantize(k, v, [0, 0])
+    q = torch.randn(B, G * H, d, generator=torch.Generator().manual_seed(13)).cuda()
+    sl = torch.tensor([pr.T - 5, 200], dtype=torch.int32, device="cuda")
+    ic, sc = pr.ctx.ip_topk(q, pr.cache, sl, H, pr.T, 64)
+    ip, sp = pr.ctx.ip_topk_paged(q, pr.pool, pr.n_blocks, pr.table, sl, H, 64)
+    assert pr.status() == tq.TQ_OK
+    assert torch.equal(ic, ip) and torch.equal(sc, sp)
 
 
 def test_block_id_outside_the_pool_is_clamped_and_reported():
