@@ -98,8 +98,9 @@ enum {
   TQ_DECODE_TC = 3,   /* tcgen05 over bit planes, e4m3 operands: d == 128, bits in {2,3},  */
                       /* group size <= 16                                                   */
   TQ_DECODE_TC4 = 4   /* tcgen05 over signed bit planes, block-scaled e2m1 operands        */
-                      /* (kind::mxf4): d == 128, bits in {2,3} with group size <= 8, and   */
-                      /* bits 4 with group size 1, 2, 4 or 8 (two query heads per pass)   */
+                      /* (kind::mxf4): d == 128, bits in {2,3} with group size <= 8 or 16  */
+                      /* (four passes of four), bits 4 with group size 1, 2, 4 or 8 (two   */
+                      /* query heads per pass)                                             */
 };
 
 /* ---- host-only set-up (no GPU needed) ------------------------------------------- */

@@ -337,7 +337,8 @@ int f4_prepare_one() {
 
 // Query heads of a KV head per kernel pass (gp, padded) and passes per KV head (split).  With
 // 4-bit codes the kernel's tensor memory holds two query heads, so a KV head with 4 or 8 runs as
-// 2 or 4 virtual KV heads of two query heads each, which read the same pages.
+// 2 or 4 virtual KV heads of two query heads each, which read the same pages; with 2 or 3 bits a
+// KV head with 16 query heads runs as 4 virtual KV heads of four.
 struct F4Shape {
   int gp, split;
 };
@@ -348,6 +349,7 @@ F4Shape f4_shape(int bits, int group) {
     if (group == 8) return {2, 4};
     return {0, 0};
   }
+  if (group == 16) return {4, 4};
   return {group <= 4 ? 4 : group <= 8 ? 8 : 0, 1};
 }
 
@@ -437,7 +439,8 @@ int prepare_decode_f4(const tq_ctx* c) {
   int rc = TQ_OK;
 #define TQ_P(BB, GG, SS) \
   if (rc == TQ_OK && c->bits == BB) rc = f4_prepare_one<BB, GG, SS>();
-  TQ_P(2, 4, 1) TQ_P(2, 8, 1) TQ_P(3, 4, 1) TQ_P(3, 8, 1) TQ_P(4, 2, 1) TQ_P(4, 2, 2) TQ_P(4, 2, 4)
+  TQ_P(2, 4, 1) TQ_P(2, 8, 1) TQ_P(3, 4, 1) TQ_P(3, 8, 1) TQ_P(2, 4, 4) TQ_P(3, 4, 4)
+  TQ_P(4, 2, 1) TQ_P(4, 2, 2) TQ_P(4, 2, 4)
 #undef TQ_P
   return rc;
 }
@@ -451,7 +454,8 @@ int launch_decode_f4(const tq_ctx* c, const MmaPlan& pl, const float* q, int bat
   if (c->bits == BB && sh.gp == GG && sh.split == SS)                                                         \
     return f4_launch_one<BB, GG, SS>(c, pl, q, batch, q_heads, kv_heads, cache, seq_lens, max_tokens, out,   \
                                      logits_out, workspace, st, pm);
-  TQ_L(2, 4, 1) TQ_L(2, 8, 1) TQ_L(3, 4, 1) TQ_L(3, 8, 1) TQ_L(4, 2, 1) TQ_L(4, 2, 2) TQ_L(4, 2, 4)
+  TQ_L(2, 4, 1) TQ_L(2, 8, 1) TQ_L(3, 4, 1) TQ_L(3, 8, 1) TQ_L(2, 4, 4) TQ_L(3, 4, 4)
+  TQ_L(4, 2, 1) TQ_L(4, 2, 2) TQ_L(4, 2, 4)
 #undef TQ_L
   return TQ_EUNSUPPORTED;
 }

@@ -96,7 +96,9 @@ def test_decode_small(d, b, G):
     ("tc4", 128, 3, 4), ("tc4", 128, 3, 8), ("tc4", 128, 2, 3), ("tc4", 128, 3, 1), ("tc4", 128, 3, 2),
     ("tc4", 128, 2, 8), ("tc4", 128, 3, 6), ("tc4", 128, 2, 5),
     # 4-bit codes: two query heads per pass, a KV head of 4 or 8 as 2 or 4 virtual ones
-    ("tc4", 128, 4, 1), ("tc4", 128, 4, 2), ("tc4", 128, 4, 4), ("tc4", 128, 4, 8)])
+    ("tc4", 128, 4, 1), ("tc4", 128, 4, 2), ("tc4", 128, 4, 4), ("tc4", 128, 4, 8),
+    # 16 query heads per KV head: four virtual KV heads of four
+    ("tc4", 128, 3, 16), ("tc4", 128, 2, 16)])
 def test_decode_small_each_kernel(path, d, b, G):
     _check_decode(d, b, G, path)
 
