@@ -84,7 +84,9 @@ struct DArgs {
   int q_heads, kv_heads, group, max_tokens, pages_per_seq, splits, pages_per_split;
 };
 
-template <int D, int BITS>
+// PAGED: pages through the block table (its own instantiation, so that the contiguous kernel
+// carries no table code)
+template <int D, int BITS, bool PAGED>
 __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
   using PL = PageLayout<D, BITS>;
   constexpr int BK = PL::BK, BV = PL::BV, LK = 1 << BK, LV = 1 << BV, KW = PL::KW;
@@ -127,13 +129,16 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
 
   const float qjl_scale = 1.2533141373155002512f / (float)PL::M;   // sqrt(pi/2) / m
   const float inv_sqrt_d = 1.0f / sqrtf((float)D);
+  const bool sparse = a.sparse_v > 0.f;   // Sparse V bookkeeping only when a threshold is set
   const size_t seq = (size_t)b * a.kv_heads + g;
   const int p0 = split * a.pages_per_split;
   const int p1 = min(p0 + a.pages_per_split, a.pages_per_seq);
 
   for (int p = p0; p < p1; ++p) {
     if (p * 128 >= seq_len) break;
-    const uint8_t* pg = a.cache + a.pm.index((int)seq, a.kv_heads, a.pages_per_seq, p, a.status) * PL::bytes;
+    const uint8_t* pg;
+    if constexpr (PAGED) pg = a.cache + a.pm.index((int)seq, a.kv_heads, a.pages_per_seq, p, a.status) * PL::bytes;
+    else pg = a.cache + (seq * a.pages_per_seq + p) * (size_t)PL::bytes;
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(pg + PL::off_kcodes);
     const uint32_t* sg = reinterpret_cast<const uint32_t*>(pg + PL::off_signs);
     const float* nk = reinterpret_cast<const float*>(pg + PL::off_nk);
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
       gmm = gm[t];
     }
     s_nv[t] = valid ? nv[t] : 0.f;
-    s_keep[t] = 0;
+    if (sparse) s_keep[t] = 0;
     for (int hc = 0; hc < G; hc += 4) {
       float am[4] = {0.f, 0.f, 0.f, 0.f}, aq[4] = {0.f, 0.f, 0.f, 0.f};
       if (valid) {
@@ -204,8 +209,10 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
         for (int i = lane; i < 128; i += 32) {
           float e = (m_new == -INFINITY) ? 0.f : expf(s_p[hh][i] - m_new);
           sum += e;   // the denominator keeps every position
-          if (e < a.sparse_v) e = 0.f;   // Sparse V: the value of this position is skipped
-          else if (e > 0.f) s_keep[i] = 1;
+          if (sparse) {   // Sparse V: the value of a position below the threshold is skipped
+            if (e < a.sparse_v) e = 0.f;
+            else if (e > 0.f) s_keep[i] = 1;
+          }
           s_p[hh][i] = e;
         }
 #pragma unroll
@@ -232,8 +239,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
 #pragma unroll
         for (int hh = 0; hh < kMaxG; ++hh)
           if (hh < G) o[hh][u] *= s_alpha[hh];
-        for (int s = 0; s < nvalid; ++s) {
-          if (!s_keep[s]) continue;   // no head keeps this position (uniform over the block)
+        auto add_slot = [&](int s) {
           int w, bit;
           slot_pos(s, w, bit);
           int idx = 0;
@@ -243,6 +249,12 @@ __global__ void __launch_bounds__(kThreads) split_kernel(DArgs a) {
 #pragma unroll
           for (int hh = 0; hh < kMaxG; ++hh)
             if (hh < G) o[hh][u] = fmaf(s_p[hh][s], val, o[hh][u]);
+        };
+        if (sparse) {   // positions no head keeps are skipped (uniform over the block)
+          for (int s = 0; s < nvalid; ++s)
+            if (s_keep[s]) add_slot(s);
+        } else {
+          for (int s = 0; s < nvalid; ++s) add_slot(s);
         }
       }
     }
@@ -326,7 +338,10 @@ int launch_d(const tq_ctx* c, const float* q, int batch, int q_heads, int kv_hea
   a.sparse_v = c->sparse_v;
   a.splits = sp.splits;
   a.pages_per_split = sp.pages_per_split;
-  split_kernel<D, BITS><<<dim3(sp.splits, kv_heads, batch), kThreads, 0, st>>>(a);
+  if (pm.table)
+    split_kernel<D, BITS, true><<<dim3(sp.splits, kv_heads, batch), kThreads, 0, st>>>(a);
+  else
+    split_kernel<D, BITS, false><<<dim3(sp.splits, kv_heads, batch), kThreads, 0, st>>>(a);
   combine_kernel<D><<<dim3(q_heads, batch), D, 0, st>>>(part, c->d_pi, out, q_heads, sp.splits);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ECUDA;
 }

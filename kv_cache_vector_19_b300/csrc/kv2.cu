@@ -480,6 +480,7 @@ __global__ void __launch_bounds__(kDThreads) split_kernel(DArgs a) {
 
   const float qjl_scale = g.m > 0 ? 1.2533141373155002512f / (float)g.m : 0.f;   // sqrt(pi/2) / m
   const float inv_sqrt_d = 1.0f / sqrtf((float)D);
+  const bool sparse = a.sparse_v > 0.f;   // Sparse V bookkeeping only when a threshold is set
   const size_t seq = (size_t)b * a.kv_heads + kvh;
   const int p0 = split * a.pages_per_split;
   const int p1 = min(p0 + a.pages_per_split, a.pages_per_seq);
@@ -504,7 +505,7 @@ __global__ void __launch_bounds__(kDThreads) split_kernel(DArgs a) {
       if (g.m > 0) gmm = gm[t];
     }
     s_nv[t] = valid ? nv[t] : 0.f;
-    s_keep[t] = 0;
+    if (sparse) s_keep[t] = 0;
     for (int hc = 0; hc < G; hc += 4) {
       float am[4] = {0.f, 0.f, 0.f, 0.f}, aq[4] = {0.f, 0.f, 0.f, 0.f};
       if (valid) {
@@ -557,8 +558,10 @@ __global__ void __launch_bounds__(kDThreads) split_kernel(DArgs a) {
         for (int i = lane; i < 128; i += 32) {
           float e = (m_new == -INFINITY) ? 0.f : expf(s_p[hh][i] - m_new);
           sum += e;   // the denominator keeps every position
-          if (e < a.sparse_v) e = 0.f;   // Sparse V: the value of this position is skipped
-          else if (e > 0.f) s_keep[i] = 1;
+          if (sparse) {   // Sparse V: the value of a position below the threshold is skipped
+            if (e < a.sparse_v) e = 0.f;
+            else if (e > 0.f) s_keep[i] = 1;
+          }
           s_p[hh][i] = e;
         }
 #pragma unroll
@@ -585,8 +588,7 @@ __global__ void __launch_bounds__(kDThreads) split_kernel(DArgs a) {
 #pragma unroll
         for (int hh = 0; hh < kMaxG; ++hh)
           if (hh < G) o[hh][u] *= s_alpha[hh];
-        for (int s = 0; s < nvalid; ++s) {
-          if (!s_keep[s]) continue;   // no head keeps this position (uniform over the block)
+        auto add_slot = [&](int s) {
           int w, bit;
           slot_pos(s, w, bit);
           int idx = 0;
@@ -596,6 +598,12 @@ __global__ void __launch_bounds__(kDThreads) split_kernel(DArgs a) {
 #pragma unroll
           for (int hh = 0; hh < kMaxG; ++hh)
             if (hh < G) o[hh][u] = fmaf(s_p[hh][s], val, o[hh][u]);
+        };
+        if (sparse) {   // positions no head keeps are skipped (uniform over the block)
+          for (int s = 0; s < nvalid; ++s)
+            if (s_keep[s]) add_slot(s);
+        } else {
+          for (int s = 0; s < nvalid; ++s) add_slot(s);
         }
       }
     }
