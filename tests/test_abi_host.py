@@ -68,3 +68,41 @@ def test_host_argument_checks_need_no_gpu():
     c = (ctypes.c_double * 4)()
     assert L.tq_make_codebook(2, 4, c, c) == tq.TQ_EINVAL
     assert L.tq_make_codebook(128, 65, c, c) == tq.TQ_EINVAL
+
+
+def test_host_argument_checks_of_the_extension_calls():
+    """Format version 2, Sparse V, strided input, the paged pool and the scan reject bad
+    arguments on the host (no GPU needed)."""
+    L = tq.lib()
+    out = ctypes.c_void_p()
+    # format version 2: widths 1..5, d in {64, 128, 256}
+    assert L.tq_ctx_create_kv(128, 7, 3, 1, 0, 0, ctypes.byref(out)) == tq.TQ_EUNSUPPORTED
+    assert L.tq_ctx_create_kv(128, 3, 0, 0, 0, 0, ctypes.byref(out)) == tq.TQ_EUNSUPPORTED
+    assert L.tq_ctx_create_kv(96, 3, 3, 1, 0, 0, ctypes.byref(out)) == tq.TQ_EUNSUPPORTED
+    assert L.tq_ctx_set_sparse_v(None, 0.1) == tq.TQ_EINVAL
+    st = (ctypes.c_int64 * 6)(0, 0, 128, 0, 0, 128)
+    assert L.tq_quantize_kv_strided(None, None, None, st, 1, 1, 1, None, None, 1, None) == tq.TQ_EINVAL
+    assert L.tq_quantize_kv_strided(None, None, None, None, 1, 1, 1, None, None, 1, None) == tq.TQ_EINVAL
+    # paged pool: a missing pool or table, no blocks or no table columns
+    assert L.tq_paged_pool_bytes(None, 1, 1) == 0
+    assert L.tq_quantize_kv_paged(None, None, None, 1, 1, 1, None, None, 1, None, 1, None) == tq.TQ_EINVAL
+    assert L.tq_quantize_kv_paged_strided(None, None, None, st, 1, 1, 1, None, None, 1, None, 1, None) == tq.TQ_EINVAL
+    assert L.tq_attn_decode_paged(None, None, 1, 1, 1, None, 1, None, 1, None, None, None, None, 0,
+                                  None) == tq.TQ_EINVAL
+    assert L.tq_dequantize_kv_paged(None, None, 1, None, 1, 1, 1, None, 1, None, None, None) == tq.TQ_EINVAL
+    # scan
+    assert L.tq_ip_topk_workspace_bytes(None, 1, 1, 1, 1) == 0
+    assert L.tq_ip_topk(None, None, 1, 1, 1, None, None, 1, 10, None, None, None, 0, None) == tq.TQ_EINVAL
+    assert L.tq_ip_topk_paged(None, None, 1, 1, 1, None, 1, None, 1, None, 10, None, None, None, 0,
+                              None) == tq.TQ_EINVAL
+
+
+def test_binding_reads_strides_of_a_token_major_view():
+    import torch
+    B, T, H, d = 2, 5, 3, 128
+    k = torch.zeros(B, T, H, d, dtype=torch.bfloat16)
+    view = k.permute(0, 2, 1, 3)   # the quantizer's [B, H, T, d] view of a projection output
+    st = tq.Context._kv_strides(view, view)
+    assert list(st) == [T * H * d, d, H * d] * 2
+    with pytest.raises(tq.TQError):
+        tq.Context._kv_strides(view.transpose(2, 3), view.transpose(2, 3))   # d not contiguous
