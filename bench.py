@@ -568,6 +568,17 @@ def run_case(args, w):
                 ctx.quantize_kv(k, v, zero, cache, T)
     if args.kernel_case == "quantize":
         call = quantize
+    elif args.kernel_case == "append":   # one token per sequence into the last slot of the prefill
+        quantize()
+        kn = torch.randn(B, H, 1, d, generator=torch.Generator().manual_seed(wl.seed + 2)).to(torch.bfloat16).cuda()
+        vn = torch.randn(B, H, 1, d, generator=torch.Generator().manual_seed(wl.seed + 3)).to(torch.bfloat16).cuda()
+        at = torch.full((B,), wl.tokens - 1, dtype=torch.int32, device="cuda")
+
+        def call():
+            if args.paged:
+                ctx.quantize_kv_paged(kn, vn, at, cache, n_blocks, table)
+            else:
+                ctx.quantize_kv(kn, vn, at, cache, T)
     else:
         quantize()
         q = (data["q"][0] * args.q_scale).cuda().contiguous()
@@ -625,7 +636,7 @@ def main():
     ap.add_argument("--workload", default="longctx", choices=["longctx", "llama8b", "llama70b", "tiny"])
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-case", choices=["quantize", "decode", "scan"], default=None,
+    ap.add_argument("--kernel-case", choices=["quantize", "decode", "scan", "append"], default=None,
                     help="run one kernel of the workload alone (profiling case), no JSON line")
     ap.add_argument("--tokens", type=int, default=0, help="prefill length of --kernel-case (default: workload's)")
     ap.add_argument("--topk", type=int, default=100, help="k of --kernel-case scan")
