@@ -38,34 +38,70 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kMaxG = 16;
 
-// q~ = Pi q and q_s = S q, one CTA of D threads per (query head, batch).
+// q~ = Pi q and q_s = S q, one CTA of 4 D threads per (query head, batch).  Thread (c, p)
+// sums the D / 16 rows k of part p for the four outputs 4c .. 4c + 3, reading Pi^T and S^T with
+// 16-byte loads (the first rows' loads issued before q arrives: the matrices are usually out of
+// L2 when a decode starts), and the 16 parts are added in shared memory.
 template <int D>
 __global__ void __launch_bounds__(4 * D) prologue_kernel(const float* __restrict__ q, const float* __restrict__ pit,
                                                          const float* __restrict__ st, float* __restrict__ qr,
                                                          float* __restrict__ qs, int q_heads) {
-  // 4 D threads: part p = tid / D sums k over its quarter of [0, D) with all of its matrix
-  // loads in flight at once (the matrices are usually out of L2 when a decode starts)
-  constexpr int KQ = D / 4;
+  constexpr int NC = D / 4, NP = 16, KP = D / NP, CH = KP < 8 ? KP : 8;   // rows per part, per chunk
   pdl_trigger();   // the decode grid may start its set-up; it waits for q~, q_s at pdl_wait
   __shared__ float sq[D];
-  __shared__ float s_a[4][D], s_s[4][D];
+  __shared__ float4 s_a[NP][NC], s_s[NP][NC];
   const size_t row = (size_t)blockIdx.y * q_heads + blockIdx.x;
-  const int j = threadIdx.x % D, part = threadIdx.x / D;
-  if (part == 0) sq[j] = q[row * D + j];
-  __syncthreads();
-  float a = 0.f, s = 0.f;
+  const int c = threadIdx.x % NC, p = threadIdx.x / NC;
+  const float4* pi4 = reinterpret_cast<const float4*>(pit);
+  const float4* st4 = reinterpret_cast<const float4*>(st);
+  float4 pa[CH], ps[CH];
 #pragma unroll
-  for (int kk = 0; kk < KQ; ++kk) {
-    const int k = part * KQ + kk;
-    a = fmaf(pit[(size_t)k * D + j], sq[k], a);   // Pi[j][k] q[k]
-    s = fmaf(st[(size_t)k * D + j], sq[k], s);    // S[j][k] q[k]
+  for (int kk = 0; kk < CH; ++kk) {
+    const int k = p * KP + kk;
+    pa[kk] = __ldg(pi4 + (size_t)k * NC + c);   // Pi[4c .. 4c+3][k]
+    ps[kk] = __ldg(st4 + (size_t)k * NC + c);   // S[4c .. 4c+3][k]
   }
-  s_a[part][j] = a;
-  s_s[part][j] = s;
+  if (threadIdx.x < D) sq[threadIdx.x] = q[row * D + threadIdx.x];
   __syncthreads();
-  if (part == 0) {
-    qr[row * D + j] = (s_a[0][j] + s_a[1][j]) + (s_a[2][j] + s_a[3][j]);
-    qs[row * D + j] = (s_s[0][j] + s_s[1][j]) + (s_s[2][j] + s_s[3][j]);
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k0 = 0; k0 < KP; k0 += CH) {
+    if (k0 > 0) {
+#pragma unroll
+      for (int kk = 0; kk < CH; ++kk) {
+        const int k = p * KP + k0 + kk;
+        pa[kk] = __ldg(pi4 + (size_t)k * NC + c);
+        ps[kk] = __ldg(st4 + (size_t)k * NC + c);
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < CH; ++kk) {
+      const float x = sq[p * KP + k0 + kk];
+      a.x = fmaf(pa[kk].x, x, a.x);
+      a.y = fmaf(pa[kk].y, x, a.y);
+      a.z = fmaf(pa[kk].z, x, a.z);
+      a.w = fmaf(pa[kk].w, x, a.w);
+      t.x = fmaf(ps[kk].x, x, t.x);
+      t.y = fmaf(ps[kk].y, x, t.y);
+      t.z = fmaf(ps[kk].z, x, t.z);
+      t.w = fmaf(ps[kk].w, x, t.w);
+    }
+  }
+  s_a[p][c] = a;
+  s_s[p][c] = t;
+  __syncthreads();
+  if (threadIdx.x < D) {
+    const int j = threadIdx.x;
+    const float* fa = reinterpret_cast<const float*>(&s_a[0][0]) + j;   // part pp at fa[pp * D]
+    const float* fs = reinterpret_cast<const float*>(&s_s[0][0]) + j;
+    float r = 0.f, u = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < NP; ++pp) {
+      r += fa[pp * D];
+      u += fs[pp * D];
+    }
+    qr[row * D + j] = r;
+    qs[row * D + j] = u;
   }
 }
 

@@ -48,9 +48,12 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
                                                          PageMap pm, KVLayout lay) {
   using PL = PageLayout<D, BITS>;
   constexpr int M = D, BK = BITS - 1, BV = BITS, LK = 1 << BK, LV = 1 << BV;
-  constexpr int NT = 4 * D, KQ = D / 4;   // 4 D threads: coordinate j, quarter qp of each sum
+  constexpr int NT = 4 * D;   // 4 D threads: coordinate j and quarter qp for the per-coordinate steps
+  // the two d x d products: thread (cg, pp) sums the KP rows of part pp for the four outputs
+  // 4 cg .. 4 cg + 3 with 16-byte loads; the 16 parts are added in shared memory
+  constexpr int NC = D / 4, NPART = 16, KP = D / NPART;
   __shared__ float s_xk[D], s_xv[D], s_r[D];
-  __shared__ float s_pa[4][D], s_pb[4][D];   // partial sums of the quarters
+  __shared__ float4 s_pa[NPART][NC], s_pb[NPART][NC];   // partial sums of the parts
   __shared__ float s_red[NT / 32];
   __shared__ uint32_t s_words[BK * PL::KW + PL::SW];   // the slot's key-code and sign words
   __shared__ int s_code[D];                            // the key's codes (exact sign decisions)
@@ -64,8 +67,9 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
   // Every fetch that does not wait for a result starts now, so that the chain below meets
   // one memory latency instead of one per step: S'^T and the near tables into L2 (the
   // projection and the near tests come later), the books into shared memory, and this
-  // thread's columns of Pi^T and S'^T into registers (head_dim <= 128; at 256 the thread budget
-  // is 64 registers and the columns are loaded in the products' loops).
+  // thread's rows of Pi^T and S'^T (four columns each, 16-byte loads) into registers
+  // (head_dim <= 128; at 256 the thread budget is 64 registers and the rows are loaded in the
+  // products' loops).
   __shared__ float s_tk[LK], s_tv[LV], s_ck[LK];
   if (threadIdx.x == 0) {
     dev::prefetch_l2(spt, (uint32_t)(D * M * sizeof(float)));
@@ -75,12 +79,15 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
   if (threadIdx.x < LV - 1) s_tv[threadIdx.x] = tv[threadIdx.x];
   if (threadIdx.x < LK) s_ck[threadIdx.x] = ck[threadIdx.x];
   constexpr bool kColumnInRegs = D <= 128;
-  float pcol[kColumnInRegs ? KQ : 1], scol[kColumnInRegs ? KQ : 1];
+  const int cg = threadIdx.x % NC, pp = threadIdx.x / NC;
+  const float4* pit4 = reinterpret_cast<const float4*>(pit);
+  const float4* spt4 = reinterpret_cast<const float4*>(spt);
+  float4 pcol[kColumnInRegs ? KP : 1], scol[kColumnInRegs ? KP : 1];
   if constexpr (kColumnInRegs) {
 #pragma unroll
-    for (int cc = 0; cc < KQ; ++cc) {
-      pcol[cc] = __ldg(pit + (size_t)(qp * KQ + cc) * D + j);
-      scol[cc] = __ldg(spt + (size_t)(qp * KQ + cc) * M + j);
+    for (int kk = 0; kk < KP; ++kk) {
+      pcol[kk] = __ldg(pit4 + (size_t)(pp * KP + kk) * NC + cg);   // Pi^T[c][4 cg .. 4 cg + 3]
+      scol[kk] = __ldg(spt4 + (size_t)(pp * KP + kk) * (M / 4) + cg);
     }
   }
   const int pos = start + t, page = pos >> 7, slot = pos & 127;
@@ -98,24 +105,32 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
   }
   const float nk = sqrtf(block_sum<NT>(xk * xk, s_red));   // also orders the s_xk / s_xv stores
   const float nv = sqrtf(block_sum<NT>(xv * xv, s_red));
-  // y_j = (Pi x)_j = sum_c Pi^T[c][j] x_c, one quarter of c per thread group, all loads in flight
+  // y_j = (Pi x)_j = sum_c Pi^T[c][j] x_c
   {
-    float pa = 0.f, pb = 0.f;
+    float4 pa = make_float4(0.f, 0.f, 0.f, 0.f), pb = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int cc = 0; cc < KQ; ++cc) {
-      const int c = qp * KQ + cc;
-      float p;
-      if constexpr (kColumnInRegs) p = pcol[cc];
-      else p = pit[(size_t)c * D + j];
-      pa = fmaf(p, s_xk[c], pa);
-      pb = fmaf(p, s_xv[c], pb);
+    for (int kk = 0; kk < KP; ++kk) {
+      const int c = pp * KP + kk;
+      float4 p4;
+      if constexpr (kColumnInRegs) p4 = pcol[kk];
+      else p4 = __ldg(pit4 + (size_t)c * NC + cg);
+      const float a = s_xk[c], w = s_xv[c];
+      pa = make_float4(fmaf(p4.x, a, pa.x), fmaf(p4.y, a, pa.y), fmaf(p4.z, a, pa.z), fmaf(p4.w, a, pa.w));
+      pb = make_float4(fmaf(p4.x, w, pb.x), fmaf(p4.y, w, pb.y), fmaf(p4.z, w, pb.z), fmaf(p4.w, w, pb.w));
     }
-    s_pa[qp][j] = pa;
-    s_pb[qp][j] = pb;
+    s_pa[pp][cg] = pa;
+    s_pb[pp][cg] = pb;
   }
   __syncthreads();
-  const float yk = (s_pa[0][j] + s_pa[1][j]) + (s_pa[2][j] + s_pa[3][j]);
-  const float yv = (s_pb[0][j] + s_pb[1][j]) + (s_pb[2][j] + s_pb[3][j]);
+  auto part_sum = [&](const float4 (*sp)[NC]) {   // sum over the parts for coordinate j
+    const float* f = reinterpret_cast<const float*>(&sp[0][0]) + j;
+    float r = 0.f;
+#pragma unroll
+    for (int q = 0; q < NPART; ++q) r += f[q * D];
+    return r;
+  };
+  const float yk = part_sum(s_pa);
+  const float yv = part_sum(s_pb);
   // Lloyd-Max codes by boundary count (a value on a boundary takes the upper code)
   const float ik = nk > 0.f ? 1.f / nk : 0.f, iv = nv > 0.f ? 1.f / nv : 0.f;
   const float uk = yk * ik, uv = yv * iv;
@@ -162,22 +177,23 @@ __global__ void __launch_bounds__(4 * D) quantize_few_kernel(const __nv_bfloat16
     s_code[j] = idx;
   }
   const float gamma = sqrtf(block_sum<NT>(qp == 0 ? r * r : 0.f, s_red));
-  // z_i = (S' Pi r)_i = sum_c S'^T[c][i] (Pi r)_c; thread (j, qp) sums quarter qp for z_j (m == d)
+  // z_i = (S' Pi r)_i = sum_c S'^T[c][i] (Pi r)_c (m == d), by parts as y
   {
-    float pz = 0.f;
+    float4 pz = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int cc = 0; cc < KQ; ++cc) {
-      const int c = qp * KQ + cc;
-      float sv;
-      if constexpr (kColumnInRegs) sv = scol[cc];
-      else sv = spt[(size_t)c * M + j];
-      pz = fmaf(sv, s_r[c], pz);
+    for (int kk = 0; kk < KP; ++kk) {
+      const int c = pp * KP + kk;
+      float4 s4;
+      if constexpr (kColumnInRegs) s4 = scol[kk];
+      else s4 = __ldg(spt4 + (size_t)c * (M / 4) + cg);
+      const float rc = s_r[c];
+      pz = make_float4(fmaf(s4.x, rc, pz.x), fmaf(s4.y, rc, pz.y), fmaf(s4.z, rc, pz.z), fmaf(s4.w, rc, pz.w));
     }
     __syncthreads();   // s_pa reads (y) done
-    s_pa[qp][j] = pz;
+    s_pa[pp][cg] = pz;
   }
   __syncthreads();
-  const float z = (s_pa[0][j] + s_pa[1][j]) + (s_pa[2][j] + s_pa[3][j]);
+  const float z = part_sum(s_pa);
   if (qp != 0) return;   // the rest is per coordinate
   // projections next to zero: exact sign
   bool sgn = z >= 0.f;
