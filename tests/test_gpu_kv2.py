@@ -16,7 +16,7 @@ import parity as P
 
 pytestmark = pytest.mark.gpu
 
-# (d, key_bits, value_bits, qjl): the VERDICT's K3V4 / K4V2 no QJL / K2V3 QJL and more shapes
+# (d, key_bits, value_bits, qjl): K3V4, K4V2 without QJL, K2V3 with QJL and more shapes
 FORMATS = [(128, 3, 4, True), (128, 4, 2, False), (128, 2, 3, True), (128, 1, 3, False), (64, 3, 3, False),
            (256, 2, 4, True), (128, 5, 5, False)]
 
