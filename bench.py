@@ -151,23 +151,19 @@ def job_gbs(world, bytes_per_rank, t_ms):
     return world * bytes_per_rank / (t_ms * 1e-3) / 1e9
 
 
-def cpu_oracle_sample(w, seconds=12.0, reps_max=1000):
-    """The oracle's own decode over packed pages (unpack + route A for the G query heads
-    of one KV head) on a 1024-token sample of the workload, repeated for ~`seconds` (half on
-    one thread, half with the BLAS pool).  Returns (GB/s of compressed pages decoded on one
-    thread, Mtokens/s quantized, threads of that figure (1), description, GB/s with the pool,
-    pool size)."""
+def _oracle_sample(w, seed):
+    """The oracle's packed pages of a 1024-token sample of workload w (one KV head) and G query
+    rows: what the CPU baseline decodes."""
     import numpy as np
+    import torch
 
-    from oracle import decode as odec
     from oracle import pagefmt, params, quant
 
-    rng = np.random.default_rng(1234)
+    rng = np.random.default_rng(seed)
     d, b, m, G = w.d, w.b, w.m, w.group
     T = 1024
     p = params.make(d, b, m, seed=w.seed)
     X = rng.standard_normal((2, T, d)).astype(np.float32)
-    import torch
     X = torch.from_numpy(X).to(torch.bfloat16).double().numpy()
     t0 = time.perf_counter()
     ok = quant.quantize_keys(X[0], p.Pi, p.S, p.cb_k)
@@ -175,40 +171,83 @@ def cpu_oracle_sample(w, seconds=12.0, reps_max=1000):
     t_quant = time.perf_counter() - t0
     pages = []
     for pg in range(T // 128):
-        s = slice(pg * 128, (pg + 1) * 128)
-        pages.append(pagefmt.pack_page(d, b, m, ok["idx"][s], ok["sigma"][s], ok["n"][s], ok["gamma"][s],
-                                       ov["idx"][s], ov["n"][s]))
-    cache = np.concatenate(pages)
-    q = rng.standard_normal((G, d))
-    def run(limit_s):
-        reps, t_dec = 0, 0.0
-        while t_dec < limit_s and reps < reps_max:
-            t0 = time.perf_counter()
-            tok = pagefmt.unpack_tokens(d, b, m, cache, T // 128, 0, 0, T, 1)
-            tk = dict(idx=tok["kidx"], n=tok["nk"].astype(np.float64), sigma=tok["sigma"],
-                      gamma=tok["gamma"].astype(np.float64))
-            tv = dict(idx=tok["vidx"], n=tok["nv"].astype(np.float64))
-            for h in range(G):
-                odec.attend_route_a(q[h], tk, tv, p.Pi, p.S, p.cb_k, p.cb_v)
-            t_dec += time.perf_counter() - t0
-            reps += 1
-        return reps * T * bpt(d, b, m) / t_dec / 1e9, reps, t_dec
+        sl = slice(pg * 128, (pg + 1) * 128)
+        pages.append(pagefmt.pack_page(d, b, m, ok["idx"][sl], ok["sigma"][sl], ok["n"][sl], ok["gamma"][sl],
+                                       ov["idx"][sl], ov["n"][sl]))
+    return dict(p=p, cache=np.concatenate(pages), q=rng.standard_normal((G, d)), T=T, t_quant=t_quant)
 
+
+def _oracle_decode(w, smp, limit_s, reps_max):
+    """Repeats the oracle decode of the sample (unpack + route A for the G query heads) for
+    ~limit_s seconds; returns (reps, seconds)."""
+    import numpy as np
+
+    from oracle import decode as odec
+    from oracle import pagefmt
+
+    d, b, m, G, T, p = w.d, w.b, w.m, w.group, smp["T"], smp["p"]
+    reps, t_dec = 0, 0.0
+    while t_dec < limit_s and reps < reps_max:
+        t0 = time.perf_counter()
+        tok = pagefmt.unpack_tokens(d, b, m, smp["cache"], T // 128, 0, 0, T, 1)
+        tk = dict(idx=tok["kidx"], n=tok["nk"].astype(np.float64), sigma=tok["sigma"],
+                  gamma=tok["gamma"].astype(np.float64))
+        tv = dict(idx=tok["vidx"], n=tok["nv"].astype(np.float64))
+        for h in range(G):
+            odec.attend_route_a(smp["q"][h], tk, tv, p.Pi, p.S, p.cb_k, p.cb_v)
+        t_dec += time.perf_counter() - t0
+        reps += 1
+    return reps, t_dec
+
+
+def _oracle_worker(job):
+    """One process of the multi-process CPU baseline: (workload name, seed, seconds) ->
+    (GB/s, reps, seconds) of the oracle decode on one thread of its own."""
+    name, seed, seconds = job
+    from threadpoolctl import threadpool_limits
+
+    from kv_cache_vector_19_b300 import workloads
+    w = workloads.preset(name)
+    with threadpool_limits(1):
+        smp = _oracle_sample(w, seed)
+        reps, t = _oracle_decode(w, smp, seconds, 10 ** 6)
+    return reps * smp["T"] * bpt(w.d, w.b, w.m) / t / 1e9, reps, t
+
+
+def cpu_oracle_sample(w, seconds=12.0, reps_max=1000, processes=0):
+    """The oracle's own decode over packed pages (unpack + route A for the G query heads of one
+    KV head) on a 1024-token sample of the workload: ~seconds / 2 on one thread, ~seconds / 2
+    with the BLAS pool, and, with processes > 1, the same sample in that many spawned processes
+    at once (one thread each; started before any GPU work).  Returns (GB/s, Mtokens/s quantized,
+    threads of the GB/s figure, description, GB/s on one thread, GB/s with the BLAS pool, pool
+    size)."""
+    smp = _oracle_sample(w, 1234)
+    T = smp["T"]
+    per_rep = T * bpt(w.d, w.b, w.m)
     try:
         from threadpoolctl import threadpool_info, threadpool_limits
         pool = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
         with threadpool_limits(1):
-            gbs1, reps1, t1 = run(seconds / 2)
+            reps1, t1 = _oracle_decode(w, smp, seconds / 2, reps_max)
     except ImportError:   # no pool control: the run below is the only figure
         threadpool_limits, pool = None, 1
-    gbs, reps, t_dec = run(seconds / 2 if threadpool_limits else seconds)
+    reps, t_dec = _oracle_decode(w, smp, seconds / 2 if threadpool_limits else seconds, reps_max)
     if threadpool_limits is None:
-        gbs1, reps1, t1 = gbs, reps, t_dec
-    desc = (f"oracle decode of 1 KV head x {T} tokens ({T // 128} packed pages) for {G} query heads: "
+        reps1, t1 = reps, t_dec
+    gbs1, gbs = reps1 * per_rep / t1 / 1e9, reps * per_rep / t_dec / 1e9
+    value, threads = gbs1, 1
+    desc = (f"oracle decode of 1 KV head x {T} tokens ({T // 128} packed pages) for {w.group} query heads: "
             f"{reps1} reps in {t1:.1f} s on 1 thread; {reps} reps in {t_dec:.1f} s with a {pool}-thread BLAS pool "
-            f"({gbs:.4f} GB/s; page unpacking is single-threaded Python either way); "
-            f"oracle quantize of {T} K+V vectors in {t_quant:.2f} s")
-    return gbs1, T / t_quant / 1e6, 1, desc, gbs, pool
+            f"({gbs:.4f} GB/s; page unpacking is single-threaded Python either way)")
+    if processes > 1 and threadpool_limits is not None:
+        import multiprocessing
+        with multiprocessing.get_context("spawn").Pool(processes) as mp:
+            res = mp.map(_oracle_worker, [(w.name, 1234 + i, seconds / 2) for i in range(processes)])
+        value, threads = sum(r[0] for r in res), processes   # the processes ran at the same time
+        desc += (f"; {processes} spawned processes at once, one thread each, {sum(r[1] for r in res)} reps "
+                 f"in ~{max(r[2] for r in res):.1f} s: {value:.4f} GB/s together")
+    desc += f"; oracle quantize of {T} K+V vectors in {smp['t_quant']:.2f} s"
+    return value, T / smp["t_quant"] / 1e6, threads, desc, gbs1, gbs, pool
 
 
 def run_reference(args, w):
@@ -220,7 +259,7 @@ def run_reference(args, w):
         cpu_oracle_sample(w, seconds=sample_s / 4, reps_max=1)
     vals, t_all = [], time.perf_counter()
     for _ in range(args.steps):
-        gbs, mtok, threads, desc, _, _ = cpu_oracle_sample(w, seconds=sample_s)
+        gbs, mtok, threads, desc, _, _, _ = cpu_oracle_sample(w, seconds=sample_s)
         vals.append(gbs)
     elapsed = time.perf_counter() - t_all
     value = statistics.mean(vals)
@@ -252,7 +291,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_sample(w)             # before any GPU work
+        cpu = cpu_oracle_sample(w, processes=min(16, os.cpu_count() or 1))   # before any GPU work
 
     torch.cuda.set_device(local)
     if world > 1:
@@ -446,9 +485,10 @@ def run_ours(args, w):
         "clocks": clk.summary(),
     }
     if cpu is not None:
-        gbs, mtok, threads, desc, gbs_pool, pool = cpu
+        gbs, mtok, threads, desc, gbs1, gbs_pool, pool = cpu
         line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
-                                "quantize_mtok_s": mtok, "value_blas_pool": gbs_pool, "blas_pool_threads": pool}
+                                "quantize_mtok_s": mtok, "value_1_thread": gbs1, "value_blas_pool": gbs_pool,
+                                "blas_pool_threads": pool}
     if rank == 0:
         print(json.dumps(line), flush=True)
     del g_dec, g_e2e
