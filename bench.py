@@ -204,13 +204,12 @@ def _oracle_worker(job):
     """One process of the multi-process CPU baseline: (workload name, seed, seconds) ->
     (GB/s, reps, seconds) of the oracle decode on one thread of its own."""
     name, seed, seconds = job
-    from threadpoolctl import threadpool_limits
-
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"   # before numpy loads its BLAS in this fresh process
     from kv_cache_vector_19_b300 import workloads
     w = workloads.preset(name)
-    with threadpool_limits(1):
-        smp = _oracle_sample(w, seed)
-        reps, t = _oracle_decode(w, smp, seconds, 10 ** 6)
+    smp = _oracle_sample(w, seed)
+    reps, t = _oracle_decode(w, smp, seconds, 10 ** 6)
     return reps * smp["T"] * bpt(w.d, w.b, w.m) / t / 1e9, reps, t
 
 
@@ -236,10 +235,14 @@ def cpu_oracle_sample(w, seconds=12.0, reps_max=1000, processes=0):
         reps1, t1 = reps, t_dec
     gbs1, gbs = reps1 * per_rep / t1 / 1e9, reps * per_rep / t_dec / 1e9
     value, threads = gbs1, 1
-    desc = (f"oracle decode of 1 KV head x {T} tokens ({T // 128} packed pages) for {w.group} query heads: "
-            f"{reps1} reps in {t1:.1f} s on 1 thread; {reps} reps in {t_dec:.1f} s with a {pool}-thread BLAS pool "
-            f"({gbs:.4f} GB/s; page unpacking is single-threaded Python either way)")
-    if processes > 1 and threadpool_limits is not None:
+    head = f"oracle decode of 1 KV head x {T} tokens ({T // 128} packed pages) for {w.group} query heads: "
+    if threadpool_limits is not None:
+        desc = head + (f"{reps1} reps in {t1:.1f} s on 1 thread; {reps} reps in {t_dec:.1f} s with a {pool}-thread "
+                       f"BLAS pool ({gbs:.4f} GB/s; page unpacking is single-threaded Python either way)")
+    else:
+        desc = head + (f"{reps} reps in {t_dec:.1f} s in this process (BLAS threads not controlled here: "
+                       f"threadpoolctl is not importable)")
+    if processes > 1:
         import multiprocessing
         with multiprocessing.get_context("spawn").Pool(processes) as mp:
             res = mp.map(_oracle_worker, [(w.name, 1234 + i, seconds / 2) for i in range(processes)])
