@@ -71,6 +71,22 @@ def attend_sparse_v(q, tok_k, tok_v, Pi, S, cb_k, cb_v, theta):
     return out, logits, skipped
 
 
+def ip_topk(q, tok_k, Pi, S, cb_k, k):
+    """Compressed inner-product scan ([BLOG] 6.4: vector search over compressed indexes): the k
+    cached keys with the largest estimated <q, k^_t> (the reconstructed key's inner product:
+    the Lloyd-Max term plus, with QJL, the sign-sketch correction), equal estimates by lower
+    slot.  Returns (slots [min(k, T)], estimates) in that order."""
+    T = len(tok_k["n"])
+    if T == 0:
+        return np.zeros(0, dtype=np.int64), np.zeros(0)
+    khat = quant.reconstruct_keys_any(tok_k, Pi, S, cb_k[0])
+    # every row summed in the same order, so that equal keys get equal estimates
+    est = np.sum(khat * np.asarray(q, dtype=np.float64)[None, :], axis=1)
+    order = sorted(range(T), key=lambda t: (-est[t], t))[:k]
+    order = np.asarray(order, dtype=np.int64)
+    return order, est[order]
+
+
 def attend_route_b(q, tok_k, tok_v, Pi, S, cb_k, cb_v):
     """Rotated-frame evaluation of the same quantities as ``attend_route_a``."""
     d = Pi.shape[0]

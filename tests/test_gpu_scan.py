@@ -6,7 +6,7 @@ compression of RAG indexes).
   estimates equal logit * sqrt(d) in fp32 — including rows whose keys repeat (ties), rows with
   one key almost everywhere (the coarse bin of the k-th key overflows shared memory and the exact
   radix select takes over), rows shorter than k (padding -1 / -inf), and k = 1 and TQ_TOPK_MAX.
-* Against the oracle (route A on the GPU's own pages, fp64): every returned estimate is within
+* Against the oracle's scan (oracle.decode.ip_topk on the GPU's own pages, fp64): every returned estimate is within
   the score bar of the oracle's, every returned slot's oracle estimate is within twice that of
   the oracle's k-th best, and every slot that beats the k-th best by more than that is returned.
 """
@@ -17,6 +17,7 @@ import pytest
 import torch
 
 import kv_cache_vector_19_b300 as tq
+from oracle import decode as odec
 import parity as P
 
 pytestmark = pytest.mark.gpu
@@ -79,10 +80,13 @@ def test_topk_matches_oracle_ranking():
     tol = 2 * P.LOGIT_ATOL * math.sqrt(d)
     for h in range(H):
         tok = run.tokens(cache, 0, h, T)
+        tk = dict(idx=tok["kidx"], n=tok["nk"].astype(np.float64), sigma=tok["sigma"],
+                  gamma=tok["gamma"].astype(np.float64))
         for gh in range(G):
             hq = h * G + gh
-            _, lo = P.oracle_logits_on_pages(run, q[0, hq].double().numpy(), tok)
-            est = lo * math.sqrt(d)
+            slots_o, est_o = odec.ip_topk(q[0, hq].double().numpy(), tk, run.p.Pi, run.p.S, run.p.cb_k, T)
+            est = np.empty(T)
+            est[slots_o] = est_o   # the oracle's estimate of every slot
             kth = np.sort(est)[::-1][k - 1]
             got = idx[0, hq]
             assert len(set(got.tolist())) == k
